@@ -1,0 +1,473 @@
+"""Benchmark of the Gated DeltaNet speculative/MTP decode step on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--graph]
+
+One step = one gdn_spec_decode call (the whole hot path: rewind, gates, q/k
+norm, recurrence, slot writes, gated RMSNorm, gather) on one batch of seeded
+synthetic inputs already resident in HBM.  Prints ONE JSON line on rank 0.
+
+Workload (default ``bs32_t8_bf16``): BS=32 sequences, H_k=2, H_v=16,
+K=V=128, T=8 draft tokens, bf16 state, acceptance U{0..8}, a 4096-slot (2 GiB)
+pool.  Eight disjoint slot tables (and eight token-input sets) rotate from
+step to step, so the state a step touches (~151 MB) was last touched 7 steps
+(~1.2 GB of traffic) earlier: the working set exceeds the 129 MB L2.
+
+Under torchrun (N > 1) each rank runs its own independent batch on its own
+GPU (sequences are independent: weak scaling, no collective on the data
+path); the timing is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "µs/step and draft-token·head updates/s at BS 4–256; % of GB300 HBM roofline"
+UNIT = "draft-token·head updates/s"
+N_SETS = 8
+
+WORKLOADS = {
+    # name: (description, constructor args)
+    "bs32_t8_bf16": ("BS=32, H_k=2, H_v=16, K=V=128, T=8, bf16 state, acceptance U{0..8}, 4096-slot (2 GiB) pool",
+                     dict(bs=32, sd="bf16")),
+    "bs32_t8_f32": ("BS=32, H_k=2, H_v=16, K=V=128, T=8, fp32 state, acceptance U{0..8}, 2048-slot (2 GiB) pool",
+                    dict(bs=32, sd="f32")),
+}
+for _bs in (4, 8, 16, 64, 128):
+    for _sd, _ns in (("bf16", 4096), ("f32", 2048)):
+        _slots = max(4 * _bs * 8, _ns, N_SETS * _bs * 8)
+        WORKLOADS[f"bs{_bs}_t8_{_sd}"] = (
+            f"BS={_bs}, H_k=2, H_v=16, K=V=128, T=8, {_sd} state, acceptance U{{0..8}}, {_slots}-slot pool",
+            dict(bs=_bs, sd=_sd))
+WORKLOADS["large_bs256_t8_bf16"] = (
+    "BS=256, H_k=4, H_v=32, K=V=128, T=8, bf16 state, acceptance Binomial(8,0.7), 16384-slot (16 GiB) pool",
+    dict(large=True))
+
+
+def make_case(name, seed):
+    from gated_deltanet_linear_sm_gb300 import synth
+    spec = WORKLOADS[name][1]
+    if spec.get("large"):
+        return synth.large(seed, num_slots=N_SETS * 256 * 8)
+    sd = {"bf16": synth.BF16, "f32": synth.F32}[spec["sd"]]
+    bs = spec["bs"]
+    ns = max(synth.sweep_num_slots(bs, 8, sd), N_SETS * bs * 8)
+    return synth.sweep(bs, sd, seed=seed, num_slots=ns)
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region (nvidia-smi, read only)
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines = []
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, f"--query-gpu={self.FIELDS}", "--format=csv,noheader",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self, which):
+        if which == "start":
+            self.t0 = time.time()
+        else:
+            self.t1 = time.time()
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        for t, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm = float(parts[1].split()[0])
+                smax = float(parts[2].split()[0])
+            except ValueError:
+                continue
+            reasons = []
+            for name, val in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"),
+                                 parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.append(name)
+            rows.append((t, sm, smax, reasons))
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        inside = [r for r in rows if self.t0 is not None and self.t0 - 0.06 <= r[0] <= (self.t1 or 1e18) + 0.06]
+        use = inside if inside else [r for r in rows if self.t0 is not None and abs(r[0] - self.t0) < 0.5] or rows
+        reasons = sorted({x for r in use for x in r[3]})
+        return {"sm_mhz": statistics.median(r[1] for r in use), "sm_max_mhz": max(r[2] for r in use),
+                "reasons": reasons, "samples": len(use), "samples_in_region": len(inside)}
+
+
+# ---------------------------------------------------------------------------
+# roofline helpers
+# ---------------------------------------------------------------------------
+
+def measured_peak_gbs():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for p in ("gated_deltanet_linear_sm_gb300/csrc/gdnspec.cu", "include/gdnspec.h"):
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload):
+    """DRAM bytes per launch from the committed ncu summary for this workload,
+    if it was taken on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", f"gdn_spec_decode_kernel_{workload}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m = re.search(r"traffic_bytes_per_launch:\s*(\d+)", text)
+    s = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
+    if not m or not s or s.group(1) != kernel_source_hash():
+        return None
+    return int(m.group(1))
+
+
+
+# ---------------------------------------------------------------------------
+# multi-rank helpers (independent batches per rank; no data-path collective)
+# ---------------------------------------------------------------------------
+
+def max_over_ranks(x, world, device):
+    """The slowest rank's time: every rank gets max(x) over the group."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_value(updates_per_rank, world, elapsed_ms_max, steps):
+    """Updates all ranks processed per second of the slowest rank's time."""
+    return updates_per_rank * world / (elapsed_ms_max * 1e-3 / steps)
+
+
+def rank_seed(rank):
+    """Each rank draws its own independent batch."""
+    return rank
+
+# ---------------------------------------------------------------------------
+# CPU arm: the oracle, timed as it stands, on the host cores
+# ---------------------------------------------------------------------------
+
+def time_oracle(case, seqs=None, min_wall=1.5, max_steps=None):
+    """Run the oracle on the given sequences of the workload (default: all)
+    repeatedly until min_wall seconds or max_steps runs; returns throughput."""
+    from gated_deltanet_linear_sm_gb300 import synth
+    from oracle import oracle as orc
+
+    threads = os.cpu_count() or 1
+    seqs = list(range(case.batch)) if seqs is None else list(seqs)
+    sub, slot_map, _ = synth.subset(case, seqs)
+    bits = case.slot_values(slot_map)
+    updates = synth.token_head_updates(sub)
+    steps = 0
+    wall = 0.0
+    while True:
+        pool = np.ascontiguousarray(bits.copy())
+        t0 = time.perf_counter()
+        orc.run_case(sub, pool, num_threads=threads)
+        wall += time.perf_counter() - t0
+        steps += 1
+        if (steps >= max_steps) if max_steps else (wall >= min_wall):
+            break
+    return {"value": updates * steps / wall, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"{steps} run(s) of {len(seqs)} of the workload's {case.batch} sequences x "
+                      f"{case.H_v} v-heads x up to 8 tokens; FP64 scalar C, OpenMP over "
+                      f"(sequence, v-head); {wall:.2f} s wall",
+            "seconds": wall, "steps": steps}
+
+
+def run_reference(args, rank, world):
+    """--impl reference: the oracle as the reference arm, rank 0 only."""
+    if rank != 0:
+        return
+    case = make_case(args.workload, seed=0)
+    # one step = the oracle on one sequence of the workload (all its v-heads
+    # and draft tokens), a bounded sample so that K steps finish in seconds
+    for _ in range(args.warmup):
+        time_oracle(case, seqs=[0], min_wall=0.0, max_steps=1)
+    r = time_oracle(case, seqs=[0], min_wall=0.0, max_steps=args.steps)
+    ms = r["seconds"] / r["steps"] * 1e3
+    line = {
+        "impl": "reference", "metric": METRIC, "value": r["value"], "unit": UNIT, "n_gpus": 0,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{args.workload}: {WORKLOADS[args.workload][0]}", "global_batch": case.batch,
+                   "seq_len": 8, "parallelism": "host cores"},
+        "cpu_baseline": {"value": r["value"], "unit": UNIT, "cores": r["cores"], "kind": "oracle",
+                         "sample": r["sample"]},
+        "e2e": {"value": r["value"], "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+
+    import gated_deltanet_linear_sm_gb300 as gdn
+    from gated_deltanet_linear_sm_gb300 import synth
+
+    gdn.load_library()                      # fail loudly if the library is missing
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    case = make_case(args.workload, seed=rank_seed(rank))
+    sets = synth.disjoint_index_sets(case, N_SETS)
+    tdt = {synth.F32: torch.float32, synth.BF16: torch.bfloat16, synth.F16: torch.float16}[case.state_dtype]
+
+    def bf(x):
+        return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    # --- resident inputs: the pool and N_SETS token-input / slot-table sets ---
+    g = torch.Generator(device=dev)
+    g.manual_seed(1000 + rank)
+    pool = torch.randn((case.num_slots, case.H_v, case.K, case.V), generator=g, device=dev, dtype=torch.float32)
+    pool = pool.mul_(0.1).to(tdt)
+    inputs = []
+    for s in range(N_SETS):
+        c = case if s == 0 else synth.make_case(
+            batch=case.batch, H_k=case.H_k, H_v=case.H_v, T=8, state_dtype=case.state_dtype,
+            num_slots=case.num_slots, acc=case.num_accepted, seed=100 * rank + s)
+        inputs.append(dict(
+            q=bf(c.q), k=bf(c.k), v=bf(c.v), a=bf(c.a), b=bf(c.b), z=bf(c.z),
+            A_log=torch.from_numpy(case.A_log).to(dev), dt_bias=bf(case.dt_bias), norm_w=bf(case.norm_w),
+            state_indices=torch.from_numpy(sets[s]).to(dev),
+            num_accepted=torch.from_numpy(case.num_accepted).to(dev),
+            cu_seqlens=torch.from_numpy(case.cu_seqlens).to(dev),
+            out=torch.zeros((case.num_tokens, case.H_v, case.V), dtype=torch.bfloat16, device=dev)))
+    calls = [gdn.prepare(t["q"], t["k"], t["v"], t["a"], t["b"], t["z"], t["A_log"], t["dt_bias"], t["norm_w"],
+                         pool, t["state_indices"], t["num_accepted"], t["cu_seqlens"], t["out"], max_T=8)
+             for t in inputs]
+    updates = synth.token_head_updates(case)
+    alg_bytes = synth.algorithmic_bytes(case)
+    stream = torch.cuda.current_stream(dev)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    # --- warm-up ---
+    for s in range(max(args.warmup, 3)):
+        calls[s % N_SETS](stream)
+    torch.cuda.synchronize()
+
+    # --- timed region: exactly K steps, device-timed with CUDA events ---
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except AttributeError:
+        gpu_id = str(local_rank)
+    sampler = ClockSampler(gpu_id)
+    sampler.start()
+    # keep the GPU busy while the sampler starts, so the timed region runs at load clocks
+    t_soak = time.time()
+    n = 0
+    while time.time() - t_soak < 0.4:
+        calls[n % N_SETS](stream)
+        n += 1
+        if n % 64 == 0:
+            torch.cuda.synchronize()
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    sampler.mark("start")
+    ev[0].record(stream)
+    for s in range(args.steps):
+        calls[s % N_SETS](stream)
+        ev[s + 1].record(stream)
+    torch.cuda.synchronize()
+    sampler.mark("end")
+    barrier()
+    torch.cuda.synchronize()
+    elapsed_ms = ev[0].elapsed_time(ev[-1])
+    per_launch = [ev[j].elapsed_time(ev[j + 1]) for j in range(args.steps)]
+    time.sleep(0.12)
+    sampler.stop()
+    clocks = sampler.summary()
+    elapsed_ms = max_over_ranks(elapsed_ms, world, dev)
+
+    # --- CUDA-graph replay variant (same K steps, one graph per slot set) ---
+    graphs = []
+    cap = torch.cuda.Stream(dev)
+    cap.wait_stream(stream)
+    for s in range(N_SETS):
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=cap):
+            calls[s](cap)
+        graphs.append(gr)
+    torch.cuda.synchronize()
+    for s in range(N_SETS):
+        graphs[s].replay()
+    torch.cuda.synchronize()
+    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    g0.record(stream)
+    for s in range(args.steps):
+        graphs[s % N_SETS].replay()
+    g1.record(stream)
+    torch.cuda.synchronize()
+    graph_ms = max_over_ranks(g0.elapsed_time(g1), world, dev)
+
+    # --- end to end through the public API with host buffers ---
+    host_sets = []
+    for t in inputs:
+        hs = {k: t[k].cpu().pin_memory() for k in ("q", "k", "v", "a", "b", "z", "state_indices",
+                                                     "num_accepted", "cu_seqlens")}
+        hs["out"] = torch.empty_like(t["out"], device="cpu").pin_memory()
+        host_sets.append(hs)
+    h2d = sum(v.numel() * v.element_size() for k, v in host_sets[0].items() if k != "out")
+    d2h = host_sets[0]["out"].numel() * host_sets[0]["out"].element_size()
+
+    def e2e_step(s):
+        hs, t = host_sets[s % N_SETS], inputs[s % N_SETS]
+        for k in ("q", "k", "v", "a", "b", "z", "state_indices", "num_accepted", "cu_seqlens"):
+            t[k].copy_(hs[k], non_blocking=True)
+        calls[s % N_SETS](stream)
+        hs["out"].copy_(t["out"], non_blocking=True)
+
+    for s in range(3):
+        e2e_step(s)
+    torch.cuda.synchronize()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for s in range(args.steps):
+        e2e_step(s)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+
+    if rank != 0:
+        return
+    ms_per_step = elapsed_ms / args.steps
+    avg_launch_ms = statistics.mean(per_launch)
+    peak, peak_kind = measured_peak_gbs()
+    achieved = alg_bytes / (avg_launch_ms * 1e-3) / 1e9
+    traffic = profiled_traffic(args.workload)
+    cpu = time_oracle(case)
+    line = {
+        "metric": METRIC,
+        "value": whole_job_value(updates, world, elapsed_ms, args.steps),
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_per_step,
+        "us_per_step": ms_per_step * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {
+            "workload": f"{args.workload}: {WORKLOADS[args.workload][0]}",
+            "global_batch": case.batch * world,
+            "seq_len": 8,
+            "parallelism": f"independent batches, {world} GPU(s)",
+            "state_dtype": synth.STATE_NAMES[case.state_dtype],
+            "cache": "rotating 8 disjoint slot tables and token-input sets; working set > L2",
+        },
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "peak_kind": f"{peak_kind} HBM copy bandwidth",
+                     "algorithmic_bytes_per_launch": alg_bytes},
+        "cpu_baseline": {k: cpu[k] for k in ("value", "unit", "cores", "kind", "sample")},
+        "e2e": {"value": whole_job_value(updates, world, e2e_ms, args.steps), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "graph_replay": {"value": whole_job_value(updates, world, graph_ms, args.steps), "unit": UNIT,
+                         "us_per_step": graph_ms * 1e3 / args.steps},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+        "split": gdn.binding.chosen_split(calls[0].dims),
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="bs32_t8_bf16")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl")
+    try:
+        run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,243 @@
+"""Python binding of libgdnspec (include/gdnspec.h): argument marshalling only.
+
+PyTorch provides device memory and streams; every step of the computation
+runs in the library's CUDA kernel.  There is no fallback: if the library has
+not been built, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+F32, BF16, F16 = 0, 1, 2
+_STATE_DTYPES = {torch.float32: F32, torch.bfloat16: BF16, torch.float16: F16}
+
+GDN_FLAG_SLOT_RANGE = 1
+GDN_FLAG_ACCEPTED = 2
+GDN_FLAG_QLEN = 4
+GDN_FLAG_TOKEN_ROW = 8
+
+
+class gdn_dims(ctypes.Structure):
+    """Mirror of gdn_dims in include/gdnspec.h."""
+
+    _fields_ = [
+        ("batch", ctypes.c_int32), ("num_tokens", ctypes.c_int32),
+        ("H_k", ctypes.c_int32), ("H_v", ctypes.c_int32),
+        ("K", ctypes.c_int32), ("V", ctypes.c_int32),
+        ("spec_stride", ctypes.c_int32), ("max_T", ctypes.c_int32),
+        ("num_slots", ctypes.c_int64),
+        ("q_stride", ctypes.c_int64), ("k_stride", ctypes.c_int64), ("v_stride", ctypes.c_int64),
+        ("a_stride", ctypes.c_int64), ("b_stride", ctypes.c_int64), ("z_stride", ctypes.c_int64),
+        ("out_stride", ctypes.c_int64),
+        ("split", ctypes.c_int32), ("reserved", ctypes.c_int32),
+    ]
+
+
+class GdnError(RuntimeError):
+    def __init__(self, status: int, text: str):
+        super().__init__(f"gdn_spec_decode failed: {text} (status {status})")
+        self.status = status
+
+
+class LibraryMissing(RuntimeError):
+    pass
+
+
+_lock = threading.Lock()
+_lib = None
+
+# the C functions and their signatures, as declared in include/gdnspec.h
+_VP = ctypes.c_void_p
+EXPORTS = {
+    "gdn_spec_decode": (ctypes.c_int, [_VP] * 15 + [ctypes.POINTER(gdn_dims), ctypes.c_float, ctypes.c_float,
+                                                   ctypes.c_int, _VP, _VP]),
+    "gdn_spec_decode_split": (ctypes.c_int32, [ctypes.POINTER(gdn_dims)]),
+    "gdn_status_str": (ctypes.c_char_p, [ctypes.c_int]),
+    "gdn_version": (ctypes.c_int32, []),
+}
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load_library() -> ctypes.CDLL:
+    """Load the in-tree libgdnspec.so (built by __graft_entry__.build() or
+    ``python -m gated_deltanet_linear_sm_gb300.build``)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = library_path()
+            if not os.path.exists(path):
+                raise LibraryMissing(f"{path} is not built; run `python -m gated_deltanet_linear_sm_gb300.build`")
+            lib = ctypes.CDLL(path)
+            for name, (res, args) in EXPORTS.items():
+                fn = getattr(lib, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = lib
+        return _lib
+
+
+def status_str(status: int) -> str:
+    return load_library().gdn_status_str(status).decode()
+
+
+def version() -> int:
+    return int(load_library().gdn_version())
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _row_stride(t, name, inner):
+    """Elements between token rows; the rest of a row must be dense."""
+    if t.dim() < 2:
+        raise ValueError(f"{name}: expected [tokens, ...]")
+    if t.dim() == 3 and (t.stride(2) != 1 or t.stride(1) != t.shape[2]):
+        raise ValueError(f"{name}: heads and head dim must be contiguous within a row")
+    if t.dim() == 2 and t.stride(1) != 1:
+        raise ValueError(f"{name}: the head dim must be contiguous")
+    return t.stride(0) if t.shape[0] > 1 else inner
+
+
+def _check(t, name, dtype, device):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if t.device != device:
+        raise ValueError(f"{name}: expected device {device}, got {t.device}")
+
+
+def make_dims(q, v, state_pool, state_indices, *, k=None, a=None, b=None, z=None, out=None,
+              max_T=None, split=0) -> gdn_dims:
+    N, H_k, K = q.shape
+    H_v, V = v.shape[1], v.shape[2]
+    batch, stride = state_indices.shape
+    d = gdn_dims()
+    d.batch, d.num_tokens, d.H_k, d.H_v, d.K, d.V = batch, N, H_k, H_v, K, V
+    d.spec_stride = stride
+    d.max_T = stride if max_T is None else max_T
+    d.num_slots = state_pool.shape[0]
+    d.q_stride = _row_stride(q, "q", H_k * K)
+    d.k_stride = _row_stride(k, "k", H_k * K) if k is not None else 0
+    d.v_stride = _row_stride(v, "v", H_v * V)
+    d.a_stride = _row_stride(a, "a", H_v) if a is not None else 0
+    d.b_stride = _row_stride(b, "b", H_v) if b is not None else 0
+    d.z_stride = _row_stride(z, "z", H_v * V) if z is not None else 0
+    d.out_stride = _row_stride(out, "out", H_v * V) if out is not None else 0
+    d.split = split
+    return d
+
+
+def gdn_spec_decode(q, k, v, a, b, z, A_log, dt_bias, norm_w, state_pool, state_indices,
+                    num_accepted, cu_seqlens, out, *, spec_token_indx=None, scale=128 ** -0.5,
+                    eps=1e-5, max_T=None, split=0, status=None, stream=None):
+    """One speculative decode step (see include/gdnspec.h).  Tensors are CUDA
+    tensors on one device: q, k [N, H_k, 128], v, z, out [N, H_v, 128], a, b
+    [N, H_v], dt_bias [H_v], norm_w [128] in bf16; A_log [H_v] fp32;
+    state_pool [num_slots, H_v, 128, 128] fp32 / bf16 / fp16 (updated in
+    place); state_indices [B, spec_stride], num_accepted [B], cu_seqlens
+    [B+1], spec_token_indx [sum q_len] (optional) and status [1] (optional)
+    int32.  Launches on ``stream`` (default: the current stream) and returns
+    ``out``."""
+    call = prepare(q, k, v, a, b, z, A_log, dt_bias, norm_w, state_pool, state_indices,
+                   num_accepted, cu_seqlens, out, spec_token_indx=spec_token_indx, scale=scale,
+                   eps=eps, max_T=max_T, split=split, status=status)
+    call(stream)
+    return out
+
+
+class PreparedCall:
+    """A marshalled gdn_spec_decode call; invoking it launches on the given
+    stream (default: the current stream), so it can be replayed in a loop or
+    captured in a CUDA graph without re-checking the arguments."""
+
+    def __init__(self, args, dims, scale, eps, state_dtype, device, keep):
+        self._fn = load_library().gdn_spec_decode
+        self._args = args
+        self._dims = dims
+        self._scale = scale
+        self._eps = eps
+        self._state_dtype = state_dtype
+        self._device = device
+        self._keep = keep          # the tensors stay alive as long as the call
+
+    @property
+    def dims(self) -> gdn_dims:
+        return self._dims
+
+    def __call__(self, stream=None):
+        if stream is None:
+            stream = torch.cuda.current_stream(self._device)
+        handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else stream
+        rc = self._fn(*self._args, ctypes.byref(self._dims), self._scale, self._eps,
+                      self._state_dtype, self._status_ptr, handle)
+        if rc != 0:
+            raise GdnError(rc, status_str(rc))
+
+    _status_ptr = None
+
+
+def prepare(q, k, v, a, b, z, A_log, dt_bias, norm_w, state_pool, state_indices, num_accepted,
+            cu_seqlens, out, *, spec_token_indx=None, scale=128 ** -0.5, eps=1e-5, max_T=None,
+            split=0, status=None) -> PreparedCall:
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("gdn_spec_decode runs on CUDA tensors only")
+    bf = torch.bfloat16
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (a, "a"), (b, "b"), (dt_bias, "dt_bias"), (out, "out")):
+        _check(t, n, bf, dev)
+    if (z is None) != (norm_w is None):
+        raise ValueError("z and norm_w must both be given or both be None")
+    if z is not None:
+        _check(z, "z", bf, dev)
+        _check(norm_w, "norm_w", bf, dev)
+        if not norm_w.is_contiguous():
+            raise ValueError("norm_w must be contiguous")
+    _check(A_log, "A_log", torch.float32, dev)
+    for t, n in ((state_indices, "state_indices"), (num_accepted, "num_accepted"), (cu_seqlens, "cu_seqlens")):
+        _check(t, n, torch.int32, dev)
+        if not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous")
+    if spec_token_indx is not None:
+        _check(spec_token_indx, "spec_token_indx", torch.int32, dev)
+        if not spec_token_indx.is_contiguous():
+            raise ValueError("spec_token_indx must be contiguous")
+    if status is not None:
+        _check(status, "status", torch.int32, dev)
+    if state_pool.dtype not in _STATE_DTYPES:
+        raise TypeError(f"state_pool: dtype {state_pool.dtype} not in fp32 / bf16 / fp16")
+    if state_pool.device != dev or not state_pool.is_contiguous():
+        raise ValueError("state_pool must be a contiguous tensor on the same device")
+    if not (A_log.is_contiguous() and dt_bias.is_contiguous()):
+        raise ValueError("A_log and dt_bias must be contiguous")
+    if q.dim() != 3 or k.shape != q.shape or v.dim() != 3 or out.shape != v.shape:
+        raise ValueError("expected q, k [N, H_k, K] and v, out [N, H_v, V]")
+    if state_indices.dim() != 2 or num_accepted.shape[0] != state_indices.shape[0] or \
+            cu_seqlens.shape[0] != state_indices.shape[0] + 1:
+        raise ValueError("expected state_indices [B, S], num_accepted [B], cu_seqlens [B+1]")
+    if state_pool.dim() != 4 or state_pool.shape[1] != v.shape[1] or state_pool.shape[2] != q.shape[2] or \
+            state_pool.shape[3] != v.shape[2]:
+        raise ValueError("expected state_pool [num_slots, H_v, K, V]")
+    dims = make_dims(q, v, state_pool, state_indices, k=k, a=a, b=b, z=z, out=out, max_T=max_T, split=split)
+    args = [_ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(b), _ptr(z), _ptr(A_log), _ptr(dt_bias), _ptr(norm_w),
+            _ptr(state_pool), _ptr(state_indices), _ptr(num_accepted), _ptr(cu_seqlens),
+            _ptr(spec_token_indx), _ptr(out)]
+    call = PreparedCall(args, dims, float(scale), float(eps), _STATE_DTYPES[state_pool.dtype], dev,
+                        keep=(q, k, v, a, b, z, A_log, dt_bias, norm_w, state_pool, state_indices,
+                              num_accepted, cu_seqlens, spec_token_indx, out, status))
+    call._status_ptr = _ptr(status)
+    return call
+
+
+def chosen_split(dims: gdn_dims) -> int:
+    return int(load_library().gdn_spec_decode_split(ctypes.byref(dims)))

@@ -1,0 +1,552 @@
+// libgdnspec: the Gated DeltaNet speculative / MTP decode step for sm_103a.
+//
+// What one call computes is stated in include/gdnspec.h, with the report
+// pages it follows.  This file holds the kernel and the C-ABI host code.
+//
+// Design (GB300):
+//  * The step is HBM-bound: one 128x128 state tile read and up to 8 tile writes
+//    per (sequence, v-head), against ~4 FP32 ops per state element per token.
+//    No tensor cores: per token it is a rank-1 update and two K-reductions.
+//  * Work unit = (sequence i, v-head h).  A warp owns 16 full V columns of the
+//    tile (all 128 K rows): lane = cg + 4*rg holds rows 16rg..16rg+15 of columns
+//    16*wg + 4cg .. +3 in 64 registers, FP32, for all draft tokens.  Because
+//    each V column evolves on its own, the two K-reductions are warp-local
+//    shuffles and the token loop has no block-level barrier.
+//  * The tile is read once with 16-byte (FP32) / 8-byte (BF16, FP16) vector
+//    loads straight into registers, all issued before the per-token prologue,
+//    so the tile read overlaps the q/k normalisation.
+//  * Both reductions use the state BEFORE the token (the "pair" reduction of
+//    the PR #51674 report, implementation step 1): with d = e^g,
+//        u = d (S^T k^),   v' = beta (v - u),   o = d (S^T q^) + (k^.q^) v'
+//    which equals o = S_new^T q^ exactly in real arithmetic.
+//  * Each token's state is stored from registers with coalesced vector
+//    stores, rounded once to the pool dtype (RNE) -- the carried state stays
+//    FP32 (PR #52191 report, implementation step 4).
+//  * Small batches: the 8 column blocks of a unit are split over SPLIT CTAs of
+//    one thread-block cluster (SPLIT = 2, 4, 8); the gated RMSNorm's
+//    mean-square over V is combined through distributed shared memory.
+//  * No device-side waits on flags, no traps: bad device data is skipped and
+//    reported through an optional status word.
+
+#include <cooperative_groups.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "gdnspec.h"
+
+namespace cg = cooperative_groups;
+
+namespace {
+
+constexpr int kK = 128;
+constexpr int kV = 128;
+constexpr int kMaxT = 8;
+constexpr int kColsPerWarp = 16;
+constexpr int kRowsPerLane = 16;
+constexpr float kQkEps = 1e-6f;              // inside the L2-norm square root
+constexpr float kSoftplusThreshold = 20.0f;  // softplus(x) = x above this
+constexpr unsigned kFull = 0xffffffffu;
+
+struct Params {
+    const __nv_bfloat16* q;
+    const __nv_bfloat16* k;
+    const __nv_bfloat16* v;
+    const __nv_bfloat16* a;
+    const __nv_bfloat16* b;
+    const __nv_bfloat16* z;
+    const float* A_log;
+    const __nv_bfloat16* dt_bias;
+    const __nv_bfloat16* norm_w;
+    void* pool;
+    const int32_t* idx;
+    const int32_t* num_acc;
+    const int32_t* cu;
+    const int32_t* sti;
+    __nv_bfloat16* out;
+    int32_t* status;
+    int64_t q_stride, k_stride, v_stride, a_stride, b_stride, z_stride, out_stride;
+    int64_t num_slots;
+    int32_t batch, num_tokens, H_k, H_v, stride, max_T, group;
+    float scale, eps;
+};
+
+// ---- state element I/O: 4 consecutive V columns of one K row ---------------
+
+template <typename T>
+struct StateIO;
+
+template <>
+struct StateIO<float> {
+    static __device__ __forceinline__ void load4(const float* p, float (&x)[4]) {
+        const float4 v = *reinterpret_cast<const float4*>(p);
+        x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
+    }
+    static __device__ __forceinline__ void store4(float* p, const float (&x)[4]) {
+        *reinterpret_cast<float4*>(p) = make_float4(x[0], x[1], x[2], x[3]);
+    }
+};
+
+template <>
+struct StateIO<__nv_bfloat16> {
+    static __device__ __forceinline__ void load4(const __nv_bfloat16* p, float (&x)[4]) {
+        const uint2 raw = *reinterpret_cast<const uint2*>(p);
+        const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.x));
+        const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.y));
+        x[0] = lo.x; x[1] = lo.y; x[2] = hi.x; x[3] = hi.y;
+    }
+    static __device__ __forceinline__ void store4(__nv_bfloat16* p, const float (&x)[4]) {
+        const __nv_bfloat162 lo = __floats2bfloat162_rn(x[0], x[1]);
+        const __nv_bfloat162 hi = __floats2bfloat162_rn(x[2], x[3]);
+        uint2 raw;
+        raw.x = *reinterpret_cast<const uint32_t*>(&lo);
+        raw.y = *reinterpret_cast<const uint32_t*>(&hi);
+        *reinterpret_cast<uint2*>(p) = raw;
+    }
+};
+
+template <>
+struct StateIO<__half> {
+    static __device__ __forceinline__ void load4(const __half* p, float (&x)[4]) {
+        const uint2 raw = *reinterpret_cast<const uint2*>(p);
+        const float2 lo = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
+        const float2 hi = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
+        x[0] = lo.x; x[1] = lo.y; x[2] = hi.x; x[3] = hi.y;
+    }
+    static __device__ __forceinline__ void store4(__half* p, const float (&x)[4]) {
+        const __half2 lo = __floats2half2_rn(x[0], x[1]);
+        const __half2 hi = __floats2half2_rn(x[2], x[3]);
+        uint2 raw;
+        raw.x = *reinterpret_cast<const uint32_t*>(&lo);
+        raw.y = *reinterpret_cast<const uint32_t*>(&hi);
+        *reinterpret_cast<uint2*>(p) = raw;
+    }
+};
+
+__device__ __forceinline__ void load_bf16x4(const __nv_bfloat16* p, float (&x)[4]) {
+    StateIO<__nv_bfloat16>::load4(p, x);
+}
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) x += __shfl_xor_sync(kFull, x, m);
+    return x;
+}
+
+__device__ __forceinline__ void raise_flag(const Params& p, int rank, int flag) {
+    if (p.status != nullptr && threadIdx.x == 0 && rank == 0) atomicOr(p.status, flag);
+}
+
+// ---- the kernel --------------------------------------------------------------
+//
+// Grid: one CTA per (unit, column slice); SPLIT CTAs of a unit form one cluster.
+// Block: W = 8 / SPLIT warps, each owning 16 of the unit's 128 V columns.
+template <typename StateT, int SPLIT>
+__global__ void __launch_bounds__(32 * (8 / SPLIT), 2 * SPLIT)
+gdn_spec_decode_kernel(const Params p) {
+    constexpr int W = 8 / SPLIT;
+    constexpr int CW = kV / SPLIT;  // V columns of this CTA
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int rank = SPLIT > 1 ? static_cast<int>(blockIdx.x % SPLIT) : 0;
+    const int unit = static_cast<int>(blockIdx.x / SPLIT);
+    const int i = unit / p.H_v;
+    const int h = unit - i * p.H_v;
+    const int cgi = lane & 3;        // column group: 4 consecutive columns
+    const int rg = lane >> 2;        // row group: 16 consecutive K rows
+    const int col0 = (rank * W + warp) * kColsPerWarp + cgi * 4;
+    const int row0 = rg * kRowsPerLane;
+
+    __shared__ __align__(16) float s_k[kMaxT][kK];
+    __shared__ __align__(16) float s_q[kMaxT][kK];
+    __shared__ __align__(16) float s_v[kMaxT][kV];
+    __shared__ __align__(16) float s_o[kMaxT][kV];
+    __shared__ float s_decay[kMaxT], s_beta[kMaxT], s_kq[kMaxT], s_red[kMaxT];
+    __shared__ int s_row[kMaxT];
+    __shared__ long long s_ws[kMaxT];
+
+    // ---- resolve the work item (every thread computes the same answer) ----
+    const int bos = p.cu[i];
+    const int q_len = p.cu[i + 1] - bos;
+    if (q_len <= 0) return;                                    // nothing to do
+    // token positions must lie inside [0, cu_seqlens[batch]), the length of
+    // spec_token_indx (rows themselves are range-checked below)
+    if (bos < 0 || bos + q_len > p.cu[p.batch]) { raise_flag(p, rank, GDN_FLAG_TOKEN_ROW); return; }
+    const int acc = p.num_acc[i];
+    if (acc > p.stride) { raise_flag(p, rank, GDN_FLAG_ACCEPTED); return; }
+    if (q_len > p.max_T || q_len > p.stride) { raise_flag(p, rank, GDN_FLAG_QLEN); return; }
+    // rewind: the state after the last accepted token; acc-1 clamped at 0
+    const long long rs = p.idx[static_cast<int64_t>(i) * p.stride + max(acc - 1, 0)];
+    if (rs < 0) return;                                        // padded sequence
+    if (rs >= p.num_slots) { raise_flag(p, rank, GDN_FLAG_SLOT_RANGE); return; }
+
+    // ---- load this lane's 16x4 block of the state tile (FP32 in registers) ----
+    constexpr int64_t kTile = static_cast<int64_t>(kK) * kV;
+    const StateT* src = static_cast<const StateT*>(p.pool) + (rs * p.H_v + h) * kTile;
+    float S[kRowsPerLane][4];
+#pragma unroll
+    for (int r = 0; r < kRowsPerLane; ++r)
+        StateIO<StateT>::load4(src + static_cast<int64_t>(row0 + r) * kV + col0, S[r]);
+
+    // ---- per-token prologue: gather rows, gates, normalised q / k, v ----
+    const int kh = h / p.group;
+    int bad = 0;
+#pragma unroll
+    for (int j = 0; j < SPLIT; ++j) {                          // W * SPLIT = 8 >= q_len
+        const int t = warp + j * W;
+        if (t < q_len) {
+            const int n = bos + t;
+            const int r = p.sti != nullptr ? p.sti[n] : n;
+            if (r < 0 || r >= p.num_tokens) {
+                bad = 1;
+            } else {
+                float qv[4], kv[4], vv[4];
+                load_bf16x4(p.q + r * p.q_stride + kh * kK + lane * 4, qv);
+                load_bf16x4(p.k + r * p.k_stride + kh * kK + lane * 4, kv);
+                load_bf16x4(p.v + r * p.v_stride + static_cast<int64_t>(h) * kV + lane * 4, vv);
+                float sq = 0.f, sk = 0.f;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) { sq += qv[e] * qv[e]; sk += kv[e] * kv[e]; }
+                sq = warp_sum(sq);
+                sk = warp_sum(sk);
+                const float rq = rsqrtf(sq + kQkEps) * p.scale;
+                const float rk = rsqrtf(sk + kQkEps);
+                float kq = 0.f;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) { qv[e] *= rq; kv[e] *= rk; kq += qv[e] * kv[e]; }
+                kq = warp_sum(kq);
+                *reinterpret_cast<float4*>(&s_q[t][lane * 4]) = make_float4(qv[0], qv[1], qv[2], qv[3]);
+                *reinterpret_cast<float4*>(&s_k[t][lane * 4]) = make_float4(kv[0], kv[1], kv[2], kv[3]);
+                *reinterpret_cast<float4*>(&s_v[t][lane * 4]) = make_float4(vv[0], vv[1], vv[2], vv[3]);
+                if (lane == 0) {
+                    const float x = __bfloat162float(p.a[r * p.a_stride + h]) + __bfloat162float(p.dt_bias[h]);
+                    const float sp = x > kSoftplusThreshold ? x : log1pf(expf(x));
+                    const float g = -expf(p.A_log[h]) * sp;
+                    s_decay[t] = expf(g);
+                    s_beta[t] = 1.0f / (1.0f + expf(-__bfloat162float(p.b[r * p.b_stride + h])));
+                    s_kq[t] = kq;
+                    s_row[t] = r;
+                    s_ws[t] = p.idx[static_cast<int64_t>(i) * p.stride + t];
+                }
+            }
+        }
+    }
+    // publishes the prologue; every CTA of the cluster checks every token row,
+    // so the skip decision below is the same in all of them
+    if (__syncthreads_or(bad)) { raise_flag(p, rank, GDN_FLAG_TOKEN_ROW); return; }
+
+    // ---- the draft tokens, in order (warp-local; no block barrier) ----
+    StateT* pool = static_cast<StateT*>(p.pool);
+    const int c_own = rg & 3;          // after the reduce-scatter: my column ...
+    const int d_own = rg >> 2;         // ... and which dot product (0: k, 1: q)
+    for (int t = 0; t < q_len; ++t) {
+        const float decay = s_decay[t];
+        const float beta = s_beta[t];
+        const float kq = s_kq[t];
+
+        // partial S^T k^ and S^T q^ over this lane's 16 rows, 4 columns each
+        float x[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] = 0.f;
+#pragma unroll
+        for (int r4 = 0; r4 < kRowsPerLane / 4; ++r4) {
+            const float4 kk = *reinterpret_cast<const float4*>(&s_k[t][row0 + 4 * r4]);
+            const float4 qq = *reinterpret_cast<const float4*>(&s_q[t][row0 + 4 * r4]);
+            const float kr[4] = {kk.x, kk.y, kk.z, kk.w};
+            const float qr[4] = {qq.x, qq.y, qq.z, qq.w};
+#pragma unroll
+            for (int rr = 0; rr < 4; ++rr)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    x[c] = fmaf(S[4 * r4 + rr][c], kr[rr], x[c]);
+                    x[4 + c] = fmaf(S[4 * r4 + rr][c], qr[rr], x[4 + c]);
+                }
+        }
+        // reduce-scatter over the 8 row groups (lane bits 4, 3, 2): afterwards
+        // lane (cg, rg) holds the full sum of value index rg = 4 d + c
+        float y[4];
+        {
+            const bool hi = (lane >> 4) & 1;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float send = hi ? x[e] : x[4 + e];
+                const float keep = hi ? x[4 + e] : x[e];
+                y[e] = keep + __shfl_xor_sync(kFull, send, 16);
+            }
+        }
+        float z2[2];
+        {
+            const bool hi = (lane >> 3) & 1;
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const float send = hi ? y[e] : y[2 + e];
+                const float keep = hi ? y[2 + e] : y[e];
+                z2[e] = keep + __shfl_xor_sync(kFull, send, 8);
+            }
+        }
+        float dot;
+        {
+            const bool hi = (lane >> 2) & 1;
+            const float send = hi ? z2[0] : z2[1];
+            const float keep = hi ? z2[1] : z2[0];
+            dot = keep + __shfl_xor_sync(kFull, send, 4);
+        }
+        // delta rule on the k lanes; readout on the q lanes
+        const float vp = beta * (s_v[t][col0 + c_own] - decay * dot);   // valid where d_own == 0
+        const float vp_pair = __shfl_xor_sync(kFull, vp, 16);
+        if (d_own == 1) s_o[t][col0 + c_own] = fmaf(decay, dot, kq * vp_pair);
+        float vpc[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) vpc[c] = __shfl_sync(kFull, vp, cgi + 4 * c);
+
+        // S <- e^g S + k^ v'^T
+#pragma unroll
+        for (int r4 = 0; r4 < kRowsPerLane / 4; ++r4) {
+            const float4 kk = *reinterpret_cast<const float4*>(&s_k[t][row0 + 4 * r4]);
+            const float kr[4] = {kk.x, kk.y, kk.z, kk.w};
+#pragma unroll
+            for (int rr = 0; rr < 4; ++rr)
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    S[4 * r4 + rr][c] = fmaf(S[4 * r4 + rr][c], decay, kr[rr] * vpc[c]);
+        }
+
+        // the state after token t goes to slot state_indices[i, t] (skip -1)
+        const long long ws = s_ws[t];
+        if (ws >= 0) {
+            if (ws < p.num_slots) {
+                StateT* dst = pool + (ws * p.H_v + h) * kTile + static_cast<int64_t>(row0) * kV + col0;
+#pragma unroll
+                for (int r = 0; r < kRowsPerLane; ++r) StateIO<StateT>::store4(dst + r * kV, S[r]);
+            } else {
+                raise_flag(p, rank, GDN_FLAG_SLOT_RANGE);
+            }
+        }
+    }
+
+    // ---- gated RMSNorm epilogue ----
+    __syncthreads();                                           // s_o of this CTA complete
+    const bool gated = p.z != nullptr;
+    if (SPLIT > 1 && gated) {
+        // partial mean-square numerators over this CTA's columns, combined
+        // across the cluster through distributed shared memory
+        for (int t = warp; t < q_len; t += W) {
+            float ss = 0.f;
+            for (int c = lane; c < CW; c += 32) {
+                const float o = s_o[t][rank * CW + c];
+                ss += o * o;
+            }
+            ss = warp_sum(ss);
+            if (lane == 0) s_red[t] = ss;
+        }
+        cg::this_cluster().sync();
+    }
+    for (int t = warp; t < q_len; t += W) {
+        float rinv = 1.0f;
+        if (gated) {
+            float ss;
+            if (SPLIT > 1) {
+                ss = 0.f;
+                cg::cluster_group cl = cg::this_cluster();
+#pragma unroll
+                for (int rr = 0; rr < SPLIT; ++rr) ss += cl.map_shared_rank(&s_red[0], rr)[t];
+            } else {
+                ss = 0.f;
+#pragma unroll
+                for (int c = 0; c < kV / 32; ++c) {
+                    const float o = s_o[t][lane + 32 * c];
+                    ss += o * o;
+                }
+                ss = warp_sum(ss);
+            }
+            rinv = rsqrtf(ss * (1.0f / kV) + p.eps);
+        }
+        if (lane < CW / 4) {
+            const int col = rank * CW + lane * 4;
+            const int r = s_row[t];
+            const float4 o4 = *reinterpret_cast<const float4*>(&s_o[t][col]);
+            float y[4] = {o4.x, o4.y, o4.z, o4.w};
+            if (gated) {
+                float zz[4], ww[4];
+                load_bf16x4(p.z + r * p.z_stride + static_cast<int64_t>(h) * kV + col, zz);
+                load_bf16x4(p.norm_w + col, ww);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) y[e] = y[e] * rinv * ww[e] * (zz[e] / (1.0f + expf(-zz[e])));
+            }
+            StateIO<__nv_bfloat16>::store4(p.out + r * p.out_stride + static_cast<int64_t>(h) * kV + col, y);
+        }
+    }
+    if (SPLIT > 1 && gated) cg::this_cluster().sync();         // peers may still read s_red
+}
+
+// ---- host side ----------------------------------------------------------------
+
+template <typename StateT, int SPLIT>
+cudaError_t launch(const Params& p, int64_t units, cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(units * SPLIT), 1, 1);
+    cfg.blockDim = dim3(32 * (8 / SPLIT), 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    cfg.numAttrs = 0;
+    if (SPLIT > 1) {
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = SPLIT;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    return cudaLaunchKernelEx(&cfg, gdn_spec_decode_kernel<StateT, SPLIT>, p);
+}
+
+template <typename StateT>
+cudaError_t launch_split(const Params& p, int64_t units, int split, cudaStream_t stream) {
+    switch (split) {
+    case 1: return launch<StateT, 1>(p, units, stream);
+    case 2: return launch<StateT, 2>(p, units, stream);
+    case 4: return launch<StateT, 4>(p, units, stream);
+    default: return launch<StateT, 8>(p, units, stream);
+    }
+}
+
+bool aligned(const void* ptr, uintptr_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }
+
+int sm_count() {
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 152;
+    if (dev < 64 && cached[dev] > 0) return cached[dev];
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 152;
+    if (dev < 64) cached[dev] = n;
+    return n;
+}
+
+// Fewest CTAs per unit that still puts about two CTAs' worth of warps on every SM.
+int choose_split(int64_t units, int sms) {
+    const int64_t target = 2 * static_cast<int64_t>(sms);
+    if (units >= target) return 1;
+    if (units * 2 >= target) return 2;
+    if (units * 4 >= target) return 4;
+    return 8;
+}
+
+gdn_status check_dims(const gdn_dims* d) {
+    if (d == nullptr) return GDN_ERR_NULL_ARG;
+    if (d->batch < 0 || d->num_tokens < 0 || d->H_k <= 0 || d->H_v <= 0 || d->spec_stride < 1 ||
+        d->num_slots < 1 || d->H_v % d->H_k != 0 || d->reserved != 0)
+        return GDN_ERR_BAD_SHAPE;
+    if (d->max_T < 1 || d->max_T > kMaxT) return GDN_ERR_BAD_SHAPE;
+    if (d->q_stride < 0 || d->k_stride < 0 || d->v_stride < 0 || d->a_stride < 0 || d->b_stride < 0 ||
+        d->z_stride < 0 || d->out_stride < 0)
+        return GDN_ERR_BAD_SHAPE;
+    if (d->K != kK || d->V != kV) return GDN_ERR_UNSUPPORTED;
+    if (!(d->split == 0 || d->split == 1 || d->split == 2 || d->split == 4 || d->split == 8))
+        return GDN_ERR_UNSUPPORTED;
+    if (static_cast<int64_t>(d->batch) * d->H_v * 8 > 0x7fffffffLL) return GDN_ERR_BAD_SHAPE;
+    return GDN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+gdn_status gdn_spec_decode(const void* q, const void* k, const void* v, const void* a, const void* b,
+                           const void* z, const float* A_log, const void* dt_bias, const void* norm_w,
+                           void* state_pool, const int32_t* state_indices, const int32_t* num_accepted,
+                           const int32_t* cu_seqlens, const int32_t* spec_token_indx, void* out,
+                           const gdn_dims* dims, float scale, float eps, gdn_dtype state_dtype,
+                           int32_t* status_word, gdn_stream_t stream) {
+    const gdn_status ds = check_dims(dims);
+    if (ds != GDN_OK) return ds;
+    if (state_dtype != GDN_F32 && state_dtype != GDN_BF16 && state_dtype != GDN_F16) return GDN_ERR_UNSUPPORTED;
+    if (dims->batch == 0) return GDN_OK;
+    if (!q || !k || !v || !a || !b || !A_log || !dt_bias || !state_pool || !state_indices || !num_accepted ||
+        !cu_seqlens || !out)
+        return GDN_ERR_NULL_ARG;
+    if ((z == nullptr) != (norm_w == nullptr)) return GDN_ERR_NULL_ARG;
+
+    const int64_t qk_row = static_cast<int64_t>(dims->H_k) * kK;
+    const int64_t v_row = static_cast<int64_t>(dims->H_v) * kV;
+    Params p;
+    p.q = static_cast<const __nv_bfloat16*>(q);
+    p.k = static_cast<const __nv_bfloat16*>(k);
+    p.v = static_cast<const __nv_bfloat16*>(v);
+    p.a = static_cast<const __nv_bfloat16*>(a);
+    p.b = static_cast<const __nv_bfloat16*>(b);
+    p.z = static_cast<const __nv_bfloat16*>(z);
+    p.A_log = A_log;
+    p.dt_bias = static_cast<const __nv_bfloat16*>(dt_bias);
+    p.norm_w = static_cast<const __nv_bfloat16*>(norm_w);
+    p.pool = state_pool;
+    p.idx = state_indices;
+    p.num_acc = num_accepted;
+    p.cu = cu_seqlens;
+    p.sti = spec_token_indx;
+    p.out = static_cast<__nv_bfloat16*>(out);
+    p.status = status_word;
+    p.q_stride = dims->q_stride ? dims->q_stride : qk_row;
+    p.k_stride = dims->k_stride ? dims->k_stride : qk_row;
+    p.v_stride = dims->v_stride ? dims->v_stride : v_row;
+    p.a_stride = dims->a_stride ? dims->a_stride : dims->H_v;
+    p.b_stride = dims->b_stride ? dims->b_stride : dims->H_v;
+    p.z_stride = dims->z_stride ? dims->z_stride : v_row;
+    p.out_stride = dims->out_stride ? dims->out_stride : v_row;
+    p.num_slots = dims->num_slots;
+    p.batch = dims->batch;
+    p.num_tokens = dims->num_tokens;
+    p.H_k = dims->H_k;
+    p.H_v = dims->H_v;
+    p.stride = dims->spec_stride;
+    p.max_T = dims->max_T;
+    p.group = dims->H_v / dims->H_k;
+    p.scale = scale;
+    p.eps = eps;
+
+    // vector accesses: 16 B state rows, 8 B bf16 quads
+    if (!aligned(state_pool, 16) || !aligned(q, 8) || !aligned(k, 8) || !aligned(v, 8) || !aligned(out, 8) ||
+        (z && !aligned(z, 8)) || (norm_w && !aligned(norm_w, 8)) || !aligned(a, 2) || !aligned(b, 2) ||
+        !aligned(dt_bias, 2) || !aligned(A_log, 4) || !aligned(state_indices, 4) || !aligned(num_accepted, 4) ||
+        !aligned(cu_seqlens, 4) || (spec_token_indx && !aligned(spec_token_indx, 4)) ||
+        (status_word && !aligned(status_word, 4)))
+        return GDN_ERR_MISALIGNED;
+    if (p.q_stride % 4 || p.k_stride % 4 || p.v_stride % 4 || p.z_stride % 4 || p.out_stride % 4)
+        return GDN_ERR_MISALIGNED;
+
+    const int64_t units = static_cast<int64_t>(dims->batch) * dims->H_v;
+    const int split = dims->split ? dims->split : choose_split(units, sm_count());
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t err;
+    switch (state_dtype) {
+    case GDN_F32: err = launch_split<float>(p, units, split, s); break;
+    case GDN_BF16: err = launch_split<__nv_bfloat16>(p, units, split, s); break;
+    default: err = launch_split<__half>(p, units, split, s); break;
+    }
+    return err == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+int32_t gdn_spec_decode_split(const gdn_dims* dims) {
+    if (check_dims(dims) != GDN_OK) return 0;
+    if (dims->split) return dims->split;
+    return choose_split(static_cast<int64_t>(dims->batch) * dims->H_v, sm_count());
+}
+
+const char* gdn_status_str(gdn_status status) {
+    switch (status) {
+    case GDN_OK: return "ok";
+    case GDN_ERR_NULL_ARG: return "a required pointer is NULL (or z / norm_w not both set)";
+    case GDN_ERR_BAD_SHAPE: return "bad sizes";
+    case GDN_ERR_UNSUPPORTED: return "unsupported head dims, state dtype or split";
+    case GDN_ERR_MISALIGNED: return "a pointer or row stride is misaligned";
+    case GDN_ERR_CUDA: return "CUDA launch failed";
+    }
+    return "unknown status";
+}
+
+int32_t gdn_version(void) { return GDNSPEC_VERSION; }
+
+}  // extern "C"

@@ -1,0 +1,175 @@
+/*
+ * libgdnspec -- the speculative / MTP decode step of a Gated DeltaNet (GDN)
+ * linear-attention layer, as hand-written CUDA for sm_103a (GB300), behind a
+ * plain C ABI.
+ *
+ * The operation follows these vLLM pull-request report pages:
+ *   "PR #51674 report -- [Kernel][Perf] Add fused CUDA post-conv MTP decode
+ *    kernel for Qwen3.5 GDN", implementation steps 1-3 and the
+ *    _custom_ops.py listing (one fused step per (request, v-head): rewind to
+ *    the last accepted state slot, up to 8 draft tokens through the gated
+ *    delta rule in order, gated RMSNorm epilogue; scale = 128^-0.5,
+ *    norm_eps = 1e-5; K = V = 128; the state is updated in place);
+ *   "PR #46090 report -- [CPU][Spec Decode] Support DFlash speculative
+ *    decoding for GDN models on CPU", implementation step 3 and the fla.cpp
+ *    listing (initial slot spec_indices[i, max(num_accepted-1, 0)], the
+ *    state after every token written to its own slot, q_len <= 0 skipped,
+ *    v-head h uses key head h / (H_v / H_k));
+ *   "PR #52191 report -- [CPU] Support FP16/BF16 persisted GDN state on
+ *    AMX", implementation steps 3-4 (arithmetic in FP32, the state stored as
+ *    FP32 / BF16 / FP16 with one rounding per slot write);
+ *   "PR #51812 report -- [Bugfix] Align Qwen GDN gates with speculative
+ *    tokens", implementation steps 1-3 (q/k/v and the a/b gates gathered with
+ *    one shared spec_token_indx in a mixed batch).
+ *
+ * Per (sequence i, v-head h), with S the K x V state (V contiguous) and
+ * r(t) the token row of draft token t:
+ *     S <- state_pool[state_indices[i, max(num_accepted[i]-1, 0)], h]
+ *     for t in 0 .. q_len-1:
+ *         g = -exp(A_log[h]) * softplus(a[r,h] + dt_bias[h]);  beta = sigmoid(b[r,h])
+ *         k^ = k[r,kh] / |k[r,kh]|;  q^ = q[r,kh] / |q[r,kh]| * scale
+ *         S <- S e^g;  v' = beta (v[r,h] - S^T k^);  S <- S + k^ v'^T;  o = S^T q^
+ *         if state_indices[i, t] >= 0: state_pool[state_indices[i, t], h] <- round(S)
+ *         out[r,h] = round_bf16( o * rsqrt(mean(o^2) + eps) * norm_w * silu(z[r,h]) )
+ * (softplus(x) = x above 20; |x| = sqrt(sum x^2 + 1e-6).)
+ *
+ * Everything here is asynchronous on the caller's stream: the library never
+ * synchronises, never reads device data on the host and allocates nothing, so
+ * a call can be captured in a CUDA graph.  All tensor pointers are
+ * caller-owned DEVICE memory (for example PyTorch tensors); the library keeps
+ * no pointer after the call returns.
+ */
+#ifndef GDNSPEC_H
+#define GDNSPEC_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define GDNSPEC_VERSION 1
+
+#if defined(__GNUC__)
+#define GDNSPEC_API __attribute__((visibility("default")))
+#else
+#define GDNSPEC_API
+#endif
+
+/* Host-side result of a call.  Nothing is launched unless GDN_OK. */
+typedef enum {
+    GDN_OK = 0,
+    GDN_ERR_NULL_ARG = 1,    /* a required pointer is NULL, or z / norm_w not both set */
+    GDN_ERR_BAD_SHAPE = 2,   /* negative sizes, H_v % H_k != 0, spec_stride < 1, max_T outside 1..8, ... */
+    GDN_ERR_UNSUPPORTED = 3, /* K != 128, V != 128, unknown state dtype, bad split */
+    GDN_ERR_MISALIGNED = 4,  /* a pointer or row stride breaks the alignment rules below */
+    GDN_ERR_CUDA = 5         /* the launch failed (the CUDA error is left for the caller to query) */
+} gdn_status;
+
+/* Element type of the recurrent-state pool. */
+typedef enum { GDN_F32 = 0, GDN_BF16 = 1, GDN_F16 = 2 } gdn_dtype;
+
+/*
+ * Bits the kernel ORs into *status_word (when given) for bad DEVICE data.
+ * The offending sequence (or, for a bad write slot, just that slot write) is
+ * skipped; nothing traps and nothing waits.
+ */
+#define GDN_FLAG_SLOT_RANGE 1  /* a read or write slot >= num_slots (read: sequence skipped; write: that write skipped) */
+#define GDN_FLAG_ACCEPTED   2  /* num_accepted[i] > spec_stride: sequence skipped */
+#define GDN_FLAG_QLEN       4  /* q_len > max_T or q_len > spec_stride: sequence skipped */
+#define GDN_FLAG_TOKEN_ROW  8  /* a token row outside [0, num_tokens), or cu_seqlens[i] < 0 or
+                                  cu_seqlens[i+1] > cu_seqlens[batch]: sequence skipped */
+
+/* Opaque CUDA stream handle; the same type as cudaStream_t (NULL = legacy default stream). */
+typedef struct CUstream_st* gdn_stream_t;
+
+/* Sizes.  All host-side integers: the launch shape never depends on device data. */
+typedef struct {
+    int32_t batch;        /* number of speculative sequences (rows of state_indices) */
+    int32_t num_tokens;   /* rows of q, k, v, a, b, z and out */
+    int32_t H_k, H_v;     /* key heads and value heads; H_v % H_k == 0 (the tuned case is H_v = 8 H_k) */
+    int32_t K, V;         /* head dims; both must be 128 */
+    int32_t spec_stride;  /* columns of state_indices (>= every q_len) */
+    int32_t max_T;        /* host-known bound on every q_len, 1..8 */
+    int64_t num_slots;    /* slots in state_pool */
+    /* Row strides between consecutive tokens, in ELEMENTS; 0 selects the dense
+       default (q, k: H_k*K; v, z, out: H_v*V; a, b: H_v).  Within a row the
+       heads are contiguous.  A packed mixed_qkv tensor [N, 2*H_k*K + H_v*V]
+       is passed as three pointers into it with q_stride = k_stride =
+       v_stride = 2*H_k*K + H_v*V. */
+    int64_t q_stride, k_stride, v_stride, a_stride, b_stride, z_stride, out_stride;
+    int32_t split;        /* CTAs per (sequence, v-head), one thread-block cluster:
+                             0 = chosen from the batch size; else 1, 2, 4 or 8 */
+    int32_t reserved;     /* must be 0 */
+} gdn_dims;
+
+/*
+ * gdn_spec_decode -- one speculative decode step over a batch.
+ *
+ * Arguments (device pointers unless stated; element types fixed):
+ *   q, k            bf16 [num_tokens, H_k, K]  (row stride q_stride / k_stride)
+ *   v               bf16 [num_tokens, H_v, V]  (row stride v_stride)
+ *   a, b            bf16 [num_tokens, H_v]     (row strides a_stride, b_stride)
+ *   z               bf16 [num_tokens, H_v, V] output gate, or NULL
+ *   A_log           fp32 [H_v]
+ *   dt_bias         bf16 [H_v]
+ *   norm_w          bf16 [V] gated-RMSNorm weight, or NULL.  z and norm_w are
+ *                   both NULL or both set; with both NULL no epilogue runs
+ *                   and out holds the raw readout o.
+ *   state_pool      state_dtype [num_slots, H_v, K, V], V contiguous; read
+ *                   and written in place
+ *   state_indices   int32 [batch, spec_stride]; -1 marks a padded slot
+ *   num_accepted    int32 [batch]; values < 1 read position 0
+ *   cu_seqlens      int32 [batch + 1]; q_len_i = cu_seqlens[i+1] - cu_seqlens[i]
+ *   spec_token_indx int32 [cu_seqlens[batch]] token row of every spec token,
+ *                   or NULL when the spec tokens are rows cu_seqlens[i] + t
+ *   out             bf16 [num_tokens, H_v, V] (row stride out_stride);
+ *                   written only at the rows of active spec tokens, other
+ *                   rows keep the caller's contents (zero-fill them first if
+ *                   padded rows flow onward, as under CUDA graphs)
+ *   dims            HOST pointer, read during the call only
+ *   scale           query scale (128^-0.5 in the pages' default)
+ *   eps             RMSNorm epsilon (1e-5 in the pages' default)
+ *   state_dtype     GDN_F32, GDN_BF16 or GDN_F16
+ *   status_word     device int32 that receives GDN_FLAG_* bits, or NULL
+ *   stream          CUDA stream to launch on
+ *
+ * Skips: q_len <= 0, or a read slot < 0 (a padded sequence), write nothing
+ * for that sequence.  A write slot < 0 skips only that write.
+ *
+ * Caller contract (not checked on the device): non-negative write slots are
+ * distinct across the batch; no sequence reads a slot that another sequence
+ * writes; token rows are used by at most one spec token.
+ *
+ * Alignment: state_pool 16 bytes; q, k, v, z, out, norm_w 8 bytes with
+ * q/k/v/z/out row strides multiples of 4 elements; int32 tables 4 bytes.
+ */
+GDNSPEC_API gdn_status gdn_spec_decode(
+    const void* q, const void* k, const void* v,
+    const void* a, const void* b, const void* z,
+    const float* A_log, const void* dt_bias, const void* norm_w,
+    void* state_pool,
+    const int32_t* state_indices, const int32_t* num_accepted,
+    const int32_t* cu_seqlens, const int32_t* spec_token_indx,
+    void* out,
+    const gdn_dims* dims, float scale, float eps, gdn_dtype state_dtype,
+    int32_t* status_word, gdn_stream_t stream);
+
+/*
+ * The CTAs per (sequence, v-head) that gdn_spec_decode would use for these
+ * sizes when dims->split == 0 (1, 2, 4 or 8), or 0 for invalid dims.  Host
+ * only; queries the current device's SM count.
+ */
+GDNSPEC_API int32_t gdn_spec_decode_split(const gdn_dims* dims);
+
+/* Static English text for a status code (never NULL). */
+GDNSPEC_API const char* gdn_status_str(gdn_status status);
+
+/* GDNSPEC_VERSION of the loaded library. */
+GDNSPEC_API int32_t gdn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDNSPEC_H */

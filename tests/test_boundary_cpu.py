@@ -1,0 +1,120 @@
+"""The C-ABI boundary without a GPU: the library loads, exports every symbol
+include/gdnspec.h declares, its ctypes mirror matches the C struct layout,
+and host-side validation rejects bad arguments before anything is launched
+(these calls return before any CUDA API is touched)."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import gated_deltanet_linear_sm_gb300 as gdn
+from gated_deltanet_linear_sm_gb300 import binding
+from gated_deltanet_linear_sm_gb300 import build as gbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gdnspec.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    gbuild.build()
+    return gdn.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return re.findall(r"GDNSPEC_API\s+[\w\s\*]+?\b(\w+)\s*\(", text)
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    assert {"gdn_spec_decode", "gdn_spec_decode_split", "gdn_status_str", "gdn_version"} <= set(names)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    assert set(declared_functions()) == set(binding.EXPORTS)
+
+
+def test_exports_are_only_the_c_abi(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", gdn.library_path()], capture_output=True, text=True)
+    if out.returncode != 0:
+        pytest.skip("nm not available")
+    ours = [l.split()[-1] for l in out.stdout.splitlines() if l.split() and l.split()[-1].startswith("gdn_")]
+    assert set(ours) == set(declared_functions())
+
+
+def test_version_and_status_strings(lib):
+    text = open(HEADER).read()
+    want = int(re.search(r"#define GDNSPEC_VERSION (\d+)", text).group(1))
+    assert gdn.version() == want
+    for code in range(6):
+        assert isinstance(gdn.status_str(code), str) and gdn.status_str(code)
+    assert gdn.status_str(99) == "unknown status"
+
+
+def test_dims_struct_layout_matches_c(tmp_path):
+    """Compile a probe against the header and compare sizeof / offsetof with
+    the ctypes mirror."""
+    fields = [f for f, _ in binding.gdn_dims._fields_]
+    src = tmp_path / "probe.c"
+    src.write_text(
+        '#include <stdio.h>\n#include <stddef.h>\n#include "gdnspec.h"\nint main(void){\n'
+        '  printf("%zu\\n", sizeof(gdn_dims));\n'
+        + "".join(f'  printf("%zu\\n", offsetof(gdn_dims, {f}));\n' for f in fields)
+        + "  return 0;\n}\n")
+    exe = tmp_path / "probe"
+    subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    vals = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()]
+    assert vals[0] == ctypes.sizeof(binding.gdn_dims)
+    for f, off in zip(fields, vals[1:]):
+        assert getattr(binding.gdn_dims, f).offset == off, f
+
+
+def _dims(**over):
+    d = binding.gdn_dims()
+    d.batch, d.num_tokens, d.H_k, d.H_v, d.K, d.V = 2, 4, 1, 8, 128, 128
+    d.spec_stride, d.max_T, d.num_slots = 2, 2, 8
+    for k, v in over.items():
+        setattr(d, k, v)
+    return d
+
+
+def _call(lib, dims, *, ptr=0x1000, z=0x1000, w=0x1000, state_dtype=0):
+    P = ptr
+    return lib.gdn_spec_decode(P, P, P, P, P, z, P, P, w, P, P, P, P, None, P,
+                               ctypes.byref(dims), 0.088, 1e-5, state_dtype, None, None)
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(K=64), 3), (dict(V=256), 3), (dict(H_v=12, H_k=8), 2), (dict(max_T=9), 2),
+    (dict(max_T=0), 2), (dict(spec_stride=0), 2), (dict(batch=-1), 2), (dict(num_slots=0), 2),
+    (dict(split=3), 3), (dict(reserved=1), 2), (dict(q_stride=-4), 2),
+])
+def test_bad_dims_rejected(lib, over, code):
+    assert _call(lib, _dims(**over)) == code
+
+
+def test_bad_pointers_and_dtype_rejected(lib):
+    assert _call(lib, _dims(), ptr=0) == 1                 # NULL tensors
+    assert _call(lib, _dims(), z=None) == 1                # z without norm_w
+    assert _call(lib, _dims(), ptr=0x1004) == 4            # pool not 16-byte aligned
+    assert _call(lib, _dims(q_stride=1026)) == 4           # q rows not 8-byte aligned
+    assert _call(lib, _dims(), state_dtype=7) == 3
+    assert lib.gdn_spec_decode(*([None] * 15), None, 0.1, 1e-5, 0, None, None) == 1
+
+
+def test_empty_batch_is_a_no_op(lib):
+    # nothing is validated beyond the sizes and nothing is launched
+    assert _call(lib, _dims(batch=0), ptr=0) == 0
+
+
+def test_explicit_split_is_reported(lib):
+    for s in (1, 2, 4, 8):
+        assert binding.chosen_split(_dims(split=s)) == s
+    assert binding.chosen_split(_dims(K=64)) == 0
