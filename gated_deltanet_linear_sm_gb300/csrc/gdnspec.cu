@@ -11,20 +11,25 @@
 //    tile (all 128 K rows): lane = cg + 4*rg holds rows 16rg..16rg+15 of columns
 //    16*wg + 4cg .. +3 in 64 registers, FP32, for all draft tokens.  Because
 //    each V column evolves on its own, the two K-reductions are warp-local
-//    shuffles and the token loop has no block-level barrier.
-//  * The tile is read once with 16-byte (FP32) / 8-byte (BF16, FP16) vector
-//    loads straight into registers, all issued before the per-token prologue,
-//    so the tile read overlaps the q/k normalisation.
+//    shuffles and the token loop needs no block barrier for the math.
+//  * Latency: every load that does not depend on another is issued up front.
+//    The tile is read straight into registers with 16-byte (FP32) / 8-byte
+//    (BF16, FP16) streaming loads before the per-token prologue, and the
+//    prologue fetches q, k, v, z, a, b and the parameters of all draft tokens
+//    at once, so the epilogue touches no global input.
 //  * Both reductions use the state BEFORE the token (the "pair" reduction of
 //    the PR #51674 report, implementation step 1): with d = e^g,
 //        u = d (S^T k^),   v' = beta (v - u),   o = d (S^T q^) + (k^.q^) v'
 //    which equals o = S_new^T q^ exactly in real arithmetic.
-//  * Each token's state is stored from registers with coalesced vector
-//    stores, rounded once to the pool dtype (RNE) -- the carried state stays
-//    FP32 (PR #52191 report, implementation step 4).
-//  * Small batches: the 8 column blocks of a unit are split over SPLIT CTAs of
+//  * Each token's state is stored from registers with streaming vector stores
+//    (each group of 4 lanes covers a contiguous 64 B / 32 B row segment),
+//    rounded once to the pool dtype (RNE) while the carried state stays FP32
+//    (PR #52191 report, implementation step 4).  Staging the tile in shared
+//    memory for full-line stores was measured slower: the per-token CTA
+//    barrier it needs costs more than the partial-line stores.
+//  * Small batches may split the 8 column blocks of a unit over SPLIT CTAs of
 //    one thread-block cluster (SPLIT = 2, 4, 8); the gated RMSNorm's
-//    mean-square over V is combined through distributed shared memory.
+//    mean-square over V is then combined through distributed shared memory.
 //  * No device-side waits on flags, no traps: bad device data is skipped and
 //    reported through an optional status word.
 
@@ -49,6 +54,12 @@ constexpr int kRowsPerLane = 16;
 constexpr float kQkEps = 1e-6f;              // inside the L2-norm square root
 constexpr float kSoftplusThreshold = 20.0f;  // softplus(x) = x above this
 constexpr unsigned kFull = 0xffffffffu;
+constexpr int64_t kTile = static_cast<int64_t>(kK) * kV;
+// k^ / q^ rows in shared memory: 4 floats of padding after every 16 rows, so
+// that the 8 row groups of a warp (16 rows = 64 B apart) land on distinct
+// banks when each reads its 16-byte chunk
+constexpr int kKPad = kK + kK / 4;
+__host__ __device__ constexpr int kpos(int row) { return row + (row >> 4) * 4; }
 
 struct Params {
     const __nv_bfloat16* q;
@@ -73,61 +84,95 @@ struct Params {
     float scale, eps;
 };
 
-// ---- state element I/O: 4 consecutive V columns of one K row ---------------
+// per-CTA shared memory
+struct alignas(16) Smem {
+    float k[kMaxT][kKPad];       // k^ per token (padded rows)
+    float q[kMaxT][kKPad];       // q^ * scale per token
+    float v[kMaxT][kV];
+    float o[kMaxT][kV];          // readout per token, for the epilogue
+    uint2 z[kMaxT][kV / 4];      // raw bf16 quads of the output gate
+    uint2 w[kV / 4];             // raw bf16 quads of norm_w
+    float decay[kMaxT], beta[kMaxT], kq[kMaxT], red[kMaxT];
+    int row[kMaxT];
+    long long ws[kMaxT];
+};
 
+template <typename StateT, int SPLIT>
+struct Config {
+    static constexpr int kWarps = 8 / SPLIT;
+    static constexpr int kThreads = 32 * kWarps;
+    static constexpr size_t kSmem = sizeof(Smem);
+};
+
+// ---- element I/O ---------------------------------------------------------------
+
+__device__ __forceinline__ void unpack_bf16x4(uint2 raw, float (&x)[4]) {
+    const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.x));
+    const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.y));
+    x[0] = lo.x; x[1] = lo.y; x[2] = hi.x; x[3] = hi.y;
+}
+
+__device__ __forceinline__ uint2 pack_bf16x4(const float (&x)[4]) {
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(x[0], x[1]);
+    const __nv_bfloat162 hi = __floats2bfloat162_rn(x[2], x[3]);
+    uint2 raw;
+    raw.x = *reinterpret_cast<const uint32_t*>(&lo);
+    raw.y = *reinterpret_cast<const uint32_t*>(&hi);
+    return raw;
+}
+
+// read-only inputs (never written by the kernel)
+__device__ __forceinline__ uint2 ldg_quad(const __nv_bfloat16* p) {
+    return __ldg(reinterpret_cast<const uint2*>(p));
+}
+
+// state tile: 4 consecutive V columns of one K row, streaming (read once /
+// written once per step)
 template <typename T>
 struct StateIO;
 
 template <>
 struct StateIO<float> {
     static __device__ __forceinline__ void load4(const float* p, float (&x)[4]) {
-        const float4 v = *reinterpret_cast<const float4*>(p);
+        const float4 v = __ldcs(reinterpret_cast<const float4*>(p));
         x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
     }
     static __device__ __forceinline__ void store4(float* p, const float (&x)[4]) {
-        *reinterpret_cast<float4*>(p) = make_float4(x[0], x[1], x[2], x[3]);
+        __stcs(reinterpret_cast<float4*>(p), make_float4(x[0], x[1], x[2], x[3]));
     }
 };
 
 template <>
 struct StateIO<__nv_bfloat16> {
     static __device__ __forceinline__ void load4(const __nv_bfloat16* p, float (&x)[4]) {
-        const uint2 raw = *reinterpret_cast<const uint2*>(p);
-        const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.x));
-        const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.y));
-        x[0] = lo.x; x[1] = lo.y; x[2] = hi.x; x[3] = hi.y;
+        unpack_bf16x4(__ldcs(reinterpret_cast<const uint2*>(p)), x);
     }
+    static __device__ __forceinline__ uint2 pack(const float (&x)[4]) { return pack_bf16x4(x); }
     static __device__ __forceinline__ void store4(__nv_bfloat16* p, const float (&x)[4]) {
-        const __nv_bfloat162 lo = __floats2bfloat162_rn(x[0], x[1]);
-        const __nv_bfloat162 hi = __floats2bfloat162_rn(x[2], x[3]);
-        uint2 raw;
-        raw.x = *reinterpret_cast<const uint32_t*>(&lo);
-        raw.y = *reinterpret_cast<const uint32_t*>(&hi);
-        *reinterpret_cast<uint2*>(p) = raw;
+        __stcs(reinterpret_cast<uint2*>(p), pack(x));
     }
 };
 
 template <>
 struct StateIO<__half> {
     static __device__ __forceinline__ void load4(const __half* p, float (&x)[4]) {
-        const uint2 raw = *reinterpret_cast<const uint2*>(p);
+        const uint2 raw = __ldcs(reinterpret_cast<const uint2*>(p));
         const float2 lo = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
         const float2 hi = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
         x[0] = lo.x; x[1] = lo.y; x[2] = hi.x; x[3] = hi.y;
     }
-    static __device__ __forceinline__ void store4(__half* p, const float (&x)[4]) {
+    static __device__ __forceinline__ uint2 pack(const float (&x)[4]) {
         const __half2 lo = __floats2half2_rn(x[0], x[1]);
         const __half2 hi = __floats2half2_rn(x[2], x[3]);
         uint2 raw;
         raw.x = *reinterpret_cast<const uint32_t*>(&lo);
         raw.y = *reinterpret_cast<const uint32_t*>(&hi);
-        *reinterpret_cast<uint2*>(p) = raw;
+        return raw;
+    }
+    static __device__ __forceinline__ void store4(__half* p, const float (&x)[4]) {
+        __stcs(reinterpret_cast<uint2*>(p), pack(x));
     }
 };
-
-__device__ __forceinline__ void load_bf16x4(const __nv_bfloat16* p, float (&x)[4]) {
-    StateIO<__nv_bfloat16>::load4(p, x);
-}
 
 __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll
@@ -142,12 +187,16 @@ __device__ __forceinline__ void raise_flag(const Params& p, int rank, int flag) 
 // ---- the kernel --------------------------------------------------------------
 //
 // Grid: one CTA per (unit, column slice); SPLIT CTAs of a unit form one cluster.
-// Block: W = 8 / SPLIT warps, each owning 16 of the unit's 128 V columns.
+// Block: 8 / SPLIT warps, each owning 16 of the unit's 128 V columns.
 template <typename StateT, int SPLIT>
-__global__ void __launch_bounds__(32 * (8 / SPLIT), 2 * SPLIT)
+__global__ void __launch_bounds__(Config<StateT, SPLIT>::kThreads, 2 * SPLIT)
 gdn_spec_decode_kernel(const Params p) {
-    constexpr int W = 8 / SPLIT;
+    using C = Config<StateT, SPLIT>;
+    constexpr int W = C::kWarps;
     constexpr int CW = kV / SPLIT;  // V columns of this CTA
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    Smem& s = *reinterpret_cast<Smem*>(smem_raw);
+
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int rank = SPLIT > 1 ? static_cast<int>(blockIdx.x % SPLIT) : 0;
@@ -156,56 +205,65 @@ gdn_spec_decode_kernel(const Params p) {
     const int h = unit - i * p.H_v;
     const int cgi = lane & 3;        // column group: 4 consecutive columns
     const int rg = lane >> 2;        // row group: 16 consecutive K rows
-    const int col0 = (rank * W + warp) * kColsPerWarp + cgi * 4;
+    const int wg = rank * W + warp;  // this warp's 16-column block (0..7)
+    const int col0 = wg * kColsPerWarp + cgi * 4;
     const int row0 = rg * kRowsPerLane;
 
-    __shared__ __align__(16) float s_k[kMaxT][kK];
-    __shared__ __align__(16) float s_q[kMaxT][kK];
-    __shared__ __align__(16) float s_v[kMaxT][kV];
-    __shared__ __align__(16) float s_o[kMaxT][kV];
-    __shared__ float s_decay[kMaxT], s_beta[kMaxT], s_kq[kMaxT], s_red[kMaxT];
-    __shared__ int s_row[kMaxT];
-    __shared__ long long s_ws[kMaxT];
-
     // ---- resolve the work item (every thread computes the same answer) ----
-    const int bos = p.cu[i];
-    const int q_len = p.cu[i + 1] - bos;
+    const int bos = __ldg(p.cu + i);
+    const int q_len = __ldg(p.cu + i + 1) - bos;
+    const int acc = __ldg(p.num_acc + i);
     if (q_len <= 0) return;                                    // nothing to do
     // token positions must lie inside [0, cu_seqlens[batch]), the length of
     // spec_token_indx (rows themselves are range-checked below)
-    if (bos < 0 || bos + q_len > p.cu[p.batch]) { raise_flag(p, rank, GDN_FLAG_TOKEN_ROW); return; }
-    const int acc = p.num_acc[i];
+    if (bos < 0 || bos + q_len > __ldg(p.cu + p.batch)) { raise_flag(p, rank, GDN_FLAG_TOKEN_ROW); return; }
     if (acc > p.stride) { raise_flag(p, rank, GDN_FLAG_ACCEPTED); return; }
     if (q_len > p.max_T || q_len > p.stride) { raise_flag(p, rank, GDN_FLAG_QLEN); return; }
     // rewind: the state after the last accepted token; acc-1 clamped at 0
-    const long long rs = p.idx[static_cast<int64_t>(i) * p.stride + max(acc - 1, 0)];
+    const long long rs = __ldg(p.idx + static_cast<int64_t>(i) * p.stride + max(acc - 1, 0));
     if (rs < 0) return;                                        // padded sequence
     if (rs >= p.num_slots) { raise_flag(p, rank, GDN_FLAG_SLOT_RANGE); return; }
 
     // ---- load this lane's 16x4 block of the state tile (FP32 in registers) ----
-    constexpr int64_t kTile = static_cast<int64_t>(kK) * kV;
     const StateT* src = static_cast<const StateT*>(p.pool) + (rs * p.H_v + h) * kTile;
     float S[kRowsPerLane][4];
 #pragma unroll
     for (int r = 0; r < kRowsPerLane; ++r)
         StateIO<StateT>::load4(src + static_cast<int64_t>(row0 + r) * kV + col0, S[r]);
 
-    // ---- per-token prologue: gather rows, gates, normalised q / k, v ----
+    // ---- per-token prologue: gather rows, gates, normalised q / k, v, z ----
     const int kh = h / p.group;
+    const bool gated = p.z != nullptr;
+    if (gated && warp == 0) s.w[lane] = ldg_quad(p.norm_w + lane * 4);
     int bad = 0;
 #pragma unroll
     for (int j = 0; j < SPLIT; ++j) {                          // W * SPLIT = 8 >= q_len
         const int t = warp + j * W;
         if (t < q_len) {
             const int n = bos + t;
-            const int r = p.sti != nullptr ? p.sti[n] : n;
+            const int r = p.sti != nullptr ? __ldg(p.sti + n) : n;
             if (r < 0 || r >= p.num_tokens) {
                 bad = 1;
             } else {
+                // every load of this token first, then the arithmetic
+                const uint2 qraw = ldg_quad(p.q + r * p.q_stride + kh * kK + lane * 4);
+                const uint2 kraw = ldg_quad(p.k + r * p.k_stride + kh * kK + lane * 4);
+                const uint2 vraw = ldg_quad(p.v + r * p.v_stride + static_cast<int64_t>(h) * kV + lane * 4);
+                uint2 zraw = make_uint2(0, 0);
+                if (gated) zraw = ldg_quad(p.z + r * p.z_stride + static_cast<int64_t>(h) * kV + lane * 4);
+                float a_in = 0.f, b_in = 0.f, dtb = 0.f, alog = 0.f;
+                long long ws = 0;
+                if (lane == 0) {
+                    a_in = __bfloat162float(p.a[r * p.a_stride + h]);
+                    b_in = __bfloat162float(p.b[r * p.b_stride + h]);
+                    dtb = __bfloat162float(p.dt_bias[h]);
+                    alog = __ldg(p.A_log + h);
+                    ws = __ldg(p.idx + static_cast<int64_t>(i) * p.stride + t);
+                }
                 float qv[4], kv[4], vv[4];
-                load_bf16x4(p.q + r * p.q_stride + kh * kK + lane * 4, qv);
-                load_bf16x4(p.k + r * p.k_stride + kh * kK + lane * 4, kv);
-                load_bf16x4(p.v + r * p.v_stride + static_cast<int64_t>(h) * kV + lane * 4, vv);
+                unpack_bf16x4(qraw, qv);
+                unpack_bf16x4(kraw, kv);
+                unpack_bf16x4(vraw, vv);
                 float sq = 0.f, sk = 0.f;
 #pragma unroll
                 for (int e = 0; e < 4; ++e) { sq += qv[e] * qv[e]; sk += kv[e] * kv[e]; }
@@ -217,18 +275,18 @@ gdn_spec_decode_kernel(const Params p) {
 #pragma unroll
                 for (int e = 0; e < 4; ++e) { qv[e] *= rq; kv[e] *= rk; kq += qv[e] * kv[e]; }
                 kq = warp_sum(kq);
-                *reinterpret_cast<float4*>(&s_q[t][lane * 4]) = make_float4(qv[0], qv[1], qv[2], qv[3]);
-                *reinterpret_cast<float4*>(&s_k[t][lane * 4]) = make_float4(kv[0], kv[1], kv[2], kv[3]);
-                *reinterpret_cast<float4*>(&s_v[t][lane * 4]) = make_float4(vv[0], vv[1], vv[2], vv[3]);
+                *reinterpret_cast<float4*>(&s.q[t][kpos(lane * 4)]) = make_float4(qv[0], qv[1], qv[2], qv[3]);
+                *reinterpret_cast<float4*>(&s.k[t][kpos(lane * 4)]) = make_float4(kv[0], kv[1], kv[2], kv[3]);
+                *reinterpret_cast<float4*>(&s.v[t][lane * 4]) = make_float4(vv[0], vv[1], vv[2], vv[3]);
+                s.z[t][lane] = zraw;
                 if (lane == 0) {
-                    const float x = __bfloat162float(p.a[r * p.a_stride + h]) + __bfloat162float(p.dt_bias[h]);
+                    const float x = a_in + dtb;
                     const float sp = x > kSoftplusThreshold ? x : log1pf(expf(x));
-                    const float g = -expf(p.A_log[h]) * sp;
-                    s_decay[t] = expf(g);
-                    s_beta[t] = 1.0f / (1.0f + expf(-__bfloat162float(p.b[r * p.b_stride + h])));
-                    s_kq[t] = kq;
-                    s_row[t] = r;
-                    s_ws[t] = p.idx[static_cast<int64_t>(i) * p.stride + t];
+                    s.decay[t] = expf(-expf(alog) * sp);
+                    s.beta[t] = 1.0f / (1.0f + expf(-b_in));
+                    s.kq[t] = kq;
+                    s.row[t] = r;
+                    s.ws[t] = ws;
                 }
             }
         }
@@ -237,14 +295,14 @@ gdn_spec_decode_kernel(const Params p) {
     // so the skip decision below is the same in all of them
     if (__syncthreads_or(bad)) { raise_flag(p, rank, GDN_FLAG_TOKEN_ROW); return; }
 
-    // ---- the draft tokens, in order (warp-local; no block barrier) ----
+    // ---- the draft tokens, in order ----
     StateT* pool = static_cast<StateT*>(p.pool);
     const int c_own = rg & 3;          // after the reduce-scatter: my column ...
     const int d_own = rg >> 2;         // ... and which dot product (0: k, 1: q)
     for (int t = 0; t < q_len; ++t) {
-        const float decay = s_decay[t];
-        const float beta = s_beta[t];
-        const float kq = s_kq[t];
+        const float decay = s.decay[t];
+        const float beta = s.beta[t];
+        const float kq = s.kq[t];
 
         // partial S^T k^ and S^T q^ over this lane's 16 rows, 4 columns each
         float x[8];
@@ -252,8 +310,8 @@ gdn_spec_decode_kernel(const Params p) {
         for (int e = 0; e < 8; ++e) x[e] = 0.f;
 #pragma unroll
         for (int r4 = 0; r4 < kRowsPerLane / 4; ++r4) {
-            const float4 kk = *reinterpret_cast<const float4*>(&s_k[t][row0 + 4 * r4]);
-            const float4 qq = *reinterpret_cast<const float4*>(&s_q[t][row0 + 4 * r4]);
+            const float4 kk = *reinterpret_cast<const float4*>(&s.k[t][kpos(row0 + 4 * r4)]);
+            const float4 qq = *reinterpret_cast<const float4*>(&s.q[t][kpos(row0 + 4 * r4)]);
             const float kr[4] = {kk.x, kk.y, kk.z, kk.w};
             const float qr[4] = {qq.x, qq.y, qq.z, qq.w};
 #pragma unroll
@@ -294,9 +352,9 @@ gdn_spec_decode_kernel(const Params p) {
             dot = keep + __shfl_xor_sync(kFull, send, 4);
         }
         // delta rule on the k lanes; readout on the q lanes
-        const float vp = beta * (s_v[t][col0 + c_own] - decay * dot);   // valid where d_own == 0
+        const float vp = beta * (s.v[t][col0 + c_own] - decay * dot);   // valid where d_own == 0
         const float vp_pair = __shfl_xor_sync(kFull, vp, 16);
-        if (d_own == 1) s_o[t][col0 + c_own] = fmaf(decay, dot, kq * vp_pair);
+        if (d_own == 1) s.o[t][col0 + c_own] = fmaf(decay, dot, kq * vp_pair);
         float vpc[4];
 #pragma unroll
         for (int c = 0; c < 4; ++c) vpc[c] = __shfl_sync(kFull, vp, cgi + 4 * c);
@@ -304,7 +362,7 @@ gdn_spec_decode_kernel(const Params p) {
         // S <- e^g S + k^ v'^T
 #pragma unroll
         for (int r4 = 0; r4 < kRowsPerLane / 4; ++r4) {
-            const float4 kk = *reinterpret_cast<const float4*>(&s_k[t][row0 + 4 * r4]);
+            const float4 kk = *reinterpret_cast<const float4*>(&s.k[t][kpos(row0 + 4 * r4)]);
             const float kr[4] = {kk.x, kk.y, kk.z, kk.w};
 #pragma unroll
             for (int rr = 0; rr < 4; ++rr)
@@ -314,49 +372,45 @@ gdn_spec_decode_kernel(const Params p) {
         }
 
         // the state after token t goes to slot state_indices[i, t] (skip -1)
-        const long long ws = s_ws[t];
-        if (ws >= 0) {
-            if (ws < p.num_slots) {
-                StateT* dst = pool + (ws * p.H_v + h) * kTile + static_cast<int64_t>(row0) * kV + col0;
+        const long long ws = s.ws[t];
+        const bool write = ws >= 0 && ws < p.num_slots;
+        if (ws >= p.num_slots) raise_flag(p, rank, GDN_FLAG_SLOT_RANGE);
+        StateT* dst = pool + (ws * p.H_v + h) * kTile;
+        if (write) {
+            StateT* d = dst + static_cast<int64_t>(row0) * kV + col0;
 #pragma unroll
-                for (int r = 0; r < kRowsPerLane; ++r) StateIO<StateT>::store4(dst + r * kV, S[r]);
-            } else {
-                raise_flag(p, rank, GDN_FLAG_SLOT_RANGE);
-            }
+            for (int r = 0; r < kRowsPerLane; ++r) StateIO<StateT>::store4(d + r * kV, S[r]);
         }
     }
 
     // ---- gated RMSNorm epilogue ----
-    __syncthreads();                                           // s_o of this CTA complete
-    const bool gated = p.z != nullptr;
+    __syncthreads();                                           // s.o of this CTA complete
     if (SPLIT > 1 && gated) {
         // partial mean-square numerators over this CTA's columns, combined
         // across the cluster through distributed shared memory
         for (int t = warp; t < q_len; t += W) {
             float ss = 0.f;
             for (int c = lane; c < CW; c += 32) {
-                const float o = s_o[t][rank * CW + c];
+                const float o = s.o[t][rank * CW + c];
                 ss += o * o;
             }
             ss = warp_sum(ss);
-            if (lane == 0) s_red[t] = ss;
+            if (lane == 0) s.red[t] = ss;
         }
         cg::this_cluster().sync();
     }
     for (int t = warp; t < q_len; t += W) {
         float rinv = 1.0f;
         if (gated) {
-            float ss;
+            float ss = 0.f;
             if (SPLIT > 1) {
-                ss = 0.f;
                 cg::cluster_group cl = cg::this_cluster();
 #pragma unroll
-                for (int rr = 0; rr < SPLIT; ++rr) ss += cl.map_shared_rank(&s_red[0], rr)[t];
+                for (int rr = 0; rr < SPLIT; ++rr) ss += cl.map_shared_rank(&s.red[0], rr)[t];
             } else {
-                ss = 0.f;
 #pragma unroll
                 for (int c = 0; c < kV / 32; ++c) {
-                    const float o = s_o[t][lane + 32 * c];
+                    const float o = s.o[t][lane + 32 * c];
                     ss += o * o;
                 }
                 ss = warp_sum(ss);
@@ -364,31 +418,48 @@ gdn_spec_decode_kernel(const Params p) {
             rinv = rsqrtf(ss * (1.0f / kV) + p.eps);
         }
         if (lane < CW / 4) {
-            const int col = rank * CW + lane * 4;
-            const int r = s_row[t];
-            const float4 o4 = *reinterpret_cast<const float4*>(&s_o[t][col]);
+            const int quad = rank * (CW / 4) + lane;
+            const int col = quad * 4;
+            const int r = s.row[t];
+            const float4 o4 = *reinterpret_cast<const float4*>(&s.o[t][col]);
             float y[4] = {o4.x, o4.y, o4.z, o4.w};
             if (gated) {
                 float zz[4], ww[4];
-                load_bf16x4(p.z + r * p.z_stride + static_cast<int64_t>(h) * kV + col, zz);
-                load_bf16x4(p.norm_w + col, ww);
+                unpack_bf16x4(s.z[t][quad], zz);
+                unpack_bf16x4(s.w[quad], ww);
 #pragma unroll
                 for (int e = 0; e < 4; ++e) y[e] = y[e] * rinv * ww[e] * (zz[e] / (1.0f + expf(-zz[e])));
             }
-            StateIO<__nv_bfloat16>::store4(p.out + r * p.out_stride + static_cast<int64_t>(h) * kV + col, y);
+            *reinterpret_cast<uint2*>(p.out + r * p.out_stride + static_cast<int64_t>(h) * kV + col) =
+                pack_bf16x4(y);
         }
     }
-    if (SPLIT > 1 && gated) cg::this_cluster().sync();         // peers may still read s_red
+    if (SPLIT > 1 && gated) cg::this_cluster().sync();         // peers may still read s.red
 }
 
 // ---- host side ----------------------------------------------------------------
 
 template <typename StateT, int SPLIT>
 cudaError_t launch(const Params& p, int64_t units, cudaStream_t stream) {
+    using C = Config<StateT, SPLIT>;
+    auto kernel = gdn_spec_decode_kernel<StateT, SPLIT>;
+    if (C::kSmem > 48 * 1024) {
+        // opt in to more than 48 KB of dynamic shared memory, once per device
+        static bool done[64] = {false};
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return e;
+        if (dev < 0 || dev >= 64 || !done[dev]) {
+            e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(C::kSmem));
+            if (e != cudaSuccess) return e;
+            if (dev >= 0 && dev < 64) done[dev] = true;
+        }
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(units * SPLIT), 1, 1);
-    cfg.blockDim = dim3(32 * (8 / SPLIT), 1, 1);
-    cfg.dynamicSmemBytes = 0;
+    cfg.blockDim = dim3(C::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = C::kSmem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     cfg.numAttrs = 0;
@@ -400,7 +471,7 @@ cudaError_t launch(const Params& p, int64_t units, cudaStream_t stream) {
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
-    return cudaLaunchKernelEx(&cfg, gdn_spec_decode_kernel<StateT, SPLIT>, p);
+    return cudaLaunchKernelEx(&cfg, kernel, p);
 }
 
 template <typename StateT>
@@ -415,25 +486,10 @@ cudaError_t launch_split(const Params& p, int64_t units, int split, cudaStream_t
 
 bool aligned(const void* ptr, uintptr_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }
 
-int sm_count() {
-    static int cached[64] = {0};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 152;
-    if (dev < 64 && cached[dev] > 0) return cached[dev];
-    int n = 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 152;
-    if (dev < 64) cached[dev] = n;
-    return n;
-}
-
-// Fewest CTAs per unit that still puts about two CTAs' worth of warps on every SM.
-int choose_split(int64_t units, int sms) {
-    const int64_t target = 2 * static_cast<int64_t>(sms);
-    if (units >= target) return 1;
-    if (units * 2 >= target) return 2;
-    if (units * 4 >= target) return 4;
-    return 8;
-}
+// One CTA per unit at every batch size measured (4 to 128 sequences of 16
+// v-heads): splitting a unit's columns over a cluster shortens no per-token
+// chain and adds cluster barriers, so the default is 1.
+int choose_split(int64_t /*units*/) { return 1; }
 
 gdn_status check_dims(const gdn_dims* d) {
     if (d == nullptr) return GDN_ERR_NULL_ARG;
@@ -518,7 +574,7 @@ gdn_status gdn_spec_decode(const void* q, const void* k, const void* v, const vo
         return GDN_ERR_MISALIGNED;
 
     const int64_t units = static_cast<int64_t>(dims->batch) * dims->H_v;
-    const int split = dims->split ? dims->split : choose_split(units, sm_count());
+    const int split = dims->split ? dims->split : choose_split(units);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t err;
     switch (state_dtype) {
@@ -532,7 +588,7 @@ gdn_status gdn_spec_decode(const void* q, const void* k, const void* v, const vo
 int32_t gdn_spec_decode_split(const gdn_dims* dims) {
     if (check_dims(dims) != GDN_OK) return 0;
     if (dims->split) return dims->split;
-    return choose_split(static_cast<int64_t>(dims->batch) * dims->H_v, sm_count());
+    return choose_split(static_cast<int64_t>(dims->batch) * dims->H_v);
 }
 
 const char* gdn_status_str(gdn_status status) {
