@@ -161,7 +161,7 @@ class PreparedCall:
     stream (default: the current stream), so it can be replayed in a loop or
     captured in a CUDA graph without re-checking the arguments."""
 
-    def __init__(self, args, dims, scale, eps, state_dtype, device, keep):
+    def __init__(self, args, dims, scale, eps, state_dtype, device, keep, status_ptr=None):
         self._fn = load_library().gdn_spec_decode
         self._args = args
         self._dims = dims
@@ -170,21 +170,25 @@ class PreparedCall:
         self._state_dtype = state_dtype
         self._device = device
         self._keep = keep          # the tensors stay alive as long as the call
+        self._status_ptr = status_ptr
+        # converted once: a call only adds the stream handle
+        self._cargs = tuple(ctypes.c_void_p(x) for x in args) + (
+            ctypes.byref(dims), ctypes.c_float(scale), ctypes.c_float(eps), ctypes.c_int(state_dtype),
+            ctypes.c_void_p(status_ptr))
 
     @property
     def dims(self) -> gdn_dims:
         return self._dims
 
     def __call__(self, stream=None):
+        """Launch on `stream`: a torch.cuda.Stream, a raw cudaStream_t handle
+        (int), or None for the current stream."""
         if stream is None:
             stream = torch.cuda.current_stream(self._device)
         handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else stream
-        rc = self._fn(*self._args, ctypes.byref(self._dims), self._scale, self._eps,
-                      self._state_dtype, self._status_ptr, handle)
+        rc = self._fn(*self._cargs, handle)
         if rc != 0:
             raise GdnError(rc, status_str(rc))
-
-    _status_ptr = None
 
 
 def prepare(q, k, v, a, b, z, A_log, dt_bias, norm_w, state_pool, state_indices, num_accepted,
@@ -232,11 +236,10 @@ def prepare(q, k, v, a, b, z, A_log, dt_bias, norm_w, state_pool, state_indices,
     args = [_ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(b), _ptr(z), _ptr(A_log), _ptr(dt_bias), _ptr(norm_w),
             _ptr(state_pool), _ptr(state_indices), _ptr(num_accepted), _ptr(cu_seqlens),
             _ptr(spec_token_indx), _ptr(out)]
-    call = PreparedCall(args, dims, float(scale), float(eps), _STATE_DTYPES[state_pool.dtype], dev,
+    return PreparedCall(args, dims, float(scale), float(eps), _STATE_DTYPES[state_pool.dtype], dev,
                         keep=(q, k, v, a, b, z, A_log, dt_bias, norm_w, state_pool, state_indices,
-                              num_accepted, cu_seqlens, spec_token_indx, out, status))
-    call._status_ptr = _ptr(status)
-    return call
+                              num_accepted, cu_seqlens, spec_token_indx, out, status),
+                        status_ptr=_ptr(status))
 
 
 def chosen_split(dims: gdn_dims) -> int:
