@@ -57,6 +57,8 @@ _VP = ctypes.c_void_p
 EXPORTS = {
     "gdn_spec_decode": (ctypes.c_int, [_VP] * 15 + [ctypes.POINTER(gdn_dims), ctypes.c_float, ctypes.c_float,
                                                    ctypes.c_int, _VP, _VP]),
+    "gdn_prefill": (ctypes.c_int, [_VP] * 14 + [ctypes.POINTER(gdn_dims), ctypes.c_float, ctypes.c_float,
+                                               ctypes.c_int, _VP, _VP]),
     "gdn_spec_decode_split": (ctypes.c_int32, [ctypes.POINTER(gdn_dims)]),
     "gdn_status_str": (ctypes.c_char_p, [ctypes.c_int]),
     "gdn_version": (ctypes.c_int32, []),
@@ -244,3 +246,49 @@ def prepare(q, k, v, a, b, z, A_log, dt_bias, norm_w, state_pool, state_indices,
 
 def chosen_split(dims: gdn_dims) -> int:
     return int(load_library().gdn_spec_decode_split(ctypes.byref(dims)))
+
+
+def gdn_prefill(q, k, v, a, b, z, A_log, dt_bias, norm_w, state_pool, read_slots, write_slots,
+                cu_seqlens, out, *, scale=128 ** -0.5, eps=1e-5, status=None, stream=None):
+    """Prefill over whole prompts (see include/gdnspec.h): sequence i is rows
+    cu_seqlens[i] .. cu_seqlens[i+1]-1 of q, k, v, a, b, z, starts from slot
+    read_slots[i] (zero state when < 0) and stores its final state in slot
+    write_slots[i] (none when < 0).  Tensors as for gdn_spec_decode;
+    read_slots, write_slots [B] int32.  Returns ``out``."""
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("gdn_prefill runs on CUDA tensors only")
+    bf = torch.bfloat16
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (a, "a"), (b, "b"), (dt_bias, "dt_bias"), (out, "out")):
+        _check(t, n, bf, dev)
+    if (z is None) != (norm_w is None):
+        raise ValueError("z and norm_w must both be given or both be None")
+    if z is not None:
+        _check(z, "z", bf, dev)
+        _check(norm_w, "norm_w", bf, dev)
+    _check(A_log, "A_log", torch.float32, dev)
+    for t, n in ((read_slots, "read_slots"), (write_slots, "write_slots"), (cu_seqlens, "cu_seqlens")):
+        _check(t, n, torch.int32, dev)
+        if not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous")
+    if read_slots.shape != write_slots.shape or read_slots.dim() != 1 or \
+            cu_seqlens.shape[0] != read_slots.shape[0] + 1:
+        raise ValueError("expected read_slots, write_slots [B] and cu_seqlens [B+1]")
+    if status is not None:
+        _check(status, "status", torch.int32, dev)
+    if state_pool.dtype not in _STATE_DTYPES or state_pool.device != dev or not state_pool.is_contiguous():
+        raise ValueError("state_pool must be a contiguous fp32 / bf16 / fp16 tensor on the same device")
+    if q.dim() != 3 or k.shape != q.shape or v.dim() != 3 or out.shape != v.shape:
+        raise ValueError("expected q, k [N, H_k, K] and v, out [N, H_v, V]")
+    # the decode-only size fields are not used by the prefill entry point
+    dims = make_dims(q, v, state_pool, read_slots.view(-1, 1), k=k, a=a, b=b, z=z, out=out, max_T=1)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else stream
+    rc = load_library().gdn_prefill(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(b), _ptr(z), _ptr(A_log), _ptr(dt_bias), _ptr(norm_w),
+        _ptr(state_pool), _ptr(read_slots), _ptr(write_slots), _ptr(cu_seqlens), _ptr(out),
+        ctypes.byref(dims), float(scale), float(eps), _STATE_DTYPES[state_pool.dtype], _ptr(status), handle)
+    if rc != 0:
+        raise GdnError(rc, status_str(rc))
+    return out

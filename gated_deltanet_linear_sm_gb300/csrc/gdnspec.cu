@@ -76,6 +76,8 @@ struct Params {
     const int32_t* num_acc;
     const int32_t* cu;
     const int32_t* sti;
+    const int32_t* read_slots;   // prefill: start slot per sequence (-1: zero state)
+    const int32_t* write_slots;  // prefill: final-state slot per sequence (-1: none)
     __nv_bfloat16* out;
     int32_t* status;
     int64_t q_stride, k_stride, v_stride, a_stride, b_stride, z_stride, out_stride;
@@ -184,211 +186,152 @@ __device__ __forceinline__ void raise_flag(const Params& p, int rank, int flag) 
     if (p.status != nullptr && threadIdx.x == 0 && rank == 0) atomicOr(p.status, flag);
 }
 
-// ---- the kernel --------------------------------------------------------------
-//
-// Grid: one CTA per (unit, column slice); SPLIT CTAs of a unit form one cluster.
-// Block: 8 / SPLIT warps, each owning 16 of the unit's 128 V columns.
-template <typename StateT, int SPLIT>
-__global__ void __launch_bounds__(Config<StateT, SPLIT>::kThreads, 2 * SPLIT)
-gdn_spec_decode_kernel(const Params p) {
-    using C = Config<StateT, SPLIT>;
-    constexpr int W = C::kWarps;
-    constexpr int CW = kV / SPLIT;  // V columns of this CTA
-    extern __shared__ __align__(16) unsigned char smem_raw[];
-    Smem& s = *reinterpret_cast<Smem*>(smem_raw);
+// ---- the pieces of one unit ------------------------------------------------------
 
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
-    const int rank = SPLIT > 1 ? static_cast<int>(blockIdx.x % SPLIT) : 0;
-    const int unit = static_cast<int>(blockIdx.x / SPLIT);
-    const int i = unit / p.H_v;
-    const int h = unit - i * p.H_v;
-    const int cgi = lane & 3;        // column group: 4 consecutive columns
-    const int rg = lane >> 2;        // row group: 16 consecutive K rows
-    const int wg = rank * W + warp;  // this warp's 16-column block (0..7)
-    const int col0 = wg * kColsPerWarp + cgi * 4;
-    const int row0 = rg * kRowsPerLane;
-
-    // ---- resolve the work item (every thread computes the same answer) ----
-    const int bos = __ldg(p.cu + i);
-    const int q_len = __ldg(p.cu + i + 1) - bos;
-    const int acc = __ldg(p.num_acc + i);
-    if (q_len <= 0) return;                                    // nothing to do
-    // token positions must lie inside [0, cu_seqlens[batch]), the length of
-    // spec_token_indx (rows themselves are range-checked below)
-    if (bos < 0 || bos + q_len > __ldg(p.cu + p.batch)) { raise_flag(p, rank, GDN_FLAG_TOKEN_ROW); return; }
-    if (acc > p.stride) { raise_flag(p, rank, GDN_FLAG_ACCEPTED); return; }
-    if (q_len > p.max_T || q_len > p.stride) { raise_flag(p, rank, GDN_FLAG_QLEN); return; }
-    // rewind: the state after the last accepted token; acc-1 clamped at 0
-    const long long rs = __ldg(p.idx + static_cast<int64_t>(i) * p.stride + max(acc - 1, 0));
-    if (rs < 0) return;                                        // padded sequence
-    if (rs >= p.num_slots) { raise_flag(p, rank, GDN_FLAG_SLOT_RANGE); return; }
-
-    // ---- load this lane's 16x4 block of the state tile (FP32 in registers) ----
-    const StateT* src = static_cast<const StateT*>(p.pool) + (rs * p.H_v + h) * kTile;
-    float S[kRowsPerLane][4];
-#pragma unroll
-    for (int r = 0; r < kRowsPerLane; ++r)
-        StateIO<StateT>::load4(src + static_cast<int64_t>(row0 + r) * kV + col0, S[r]);
-
-    // ---- per-token prologue: gather rows, gates, normalised q / k, v, z ----
-    const int kh = h / p.group;
-    const bool gated = p.z != nullptr;
-    if (gated && warp == 0) s.w[lane] = ldg_quad(p.norm_w + lane * 4);
-    int bad = 0;
-#pragma unroll
-    for (int j = 0; j < SPLIT; ++j) {                          // W * SPLIT = 8 >= q_len
-        const int t = warp + j * W;
-        if (t < q_len) {
-            const int n = bos + t;
-            const int r = p.sti != nullptr ? __ldg(p.sti + n) : n;
-            if (r < 0 || r >= p.num_tokens) {
-                bad = 1;
-            } else {
-                // every load of this token first, then the arithmetic
-                const uint2 qraw = ldg_quad(p.q + r * p.q_stride + kh * kK + lane * 4);
-                const uint2 kraw = ldg_quad(p.k + r * p.k_stride + kh * kK + lane * 4);
-                const uint2 vraw = ldg_quad(p.v + r * p.v_stride + static_cast<int64_t>(h) * kV + lane * 4);
-                uint2 zraw = make_uint2(0, 0);
-                if (gated) zraw = ldg_quad(p.z + r * p.z_stride + static_cast<int64_t>(h) * kV + lane * 4);
-                float a_in = 0.f, b_in = 0.f, dtb = 0.f, alog = 0.f;
-                long long ws = 0;
-                if (lane == 0) {
-                    a_in = __bfloat162float(p.a[r * p.a_stride + h]);
-                    b_in = __bfloat162float(p.b[r * p.b_stride + h]);
-                    dtb = __bfloat162float(p.dt_bias[h]);
-                    alog = __ldg(p.A_log + h);
-                    ws = __ldg(p.idx + static_cast<int64_t>(i) * p.stride + t);
-                }
-                float qv[4], kv[4], vv[4];
-                unpack_bf16x4(qraw, qv);
-                unpack_bf16x4(kraw, kv);
-                unpack_bf16x4(vraw, vv);
-                float sq = 0.f, sk = 0.f;
-#pragma unroll
-                for (int e = 0; e < 4; ++e) { sq += qv[e] * qv[e]; sk += kv[e] * kv[e]; }
-                sq = warp_sum(sq);
-                sk = warp_sum(sk);
-                const float rq = rsqrtf(sq + kQkEps) * p.scale;
-                const float rk = rsqrtf(sk + kQkEps);
-                float kq = 0.f;
-#pragma unroll
-                for (int e = 0; e < 4; ++e) { qv[e] *= rq; kv[e] *= rk; kq += qv[e] * kv[e]; }
-                kq = warp_sum(kq);
-                *reinterpret_cast<float4*>(&s.q[t][kpos(lane * 4)]) = make_float4(qv[0], qv[1], qv[2], qv[3]);
-                *reinterpret_cast<float4*>(&s.k[t][kpos(lane * 4)]) = make_float4(kv[0], kv[1], kv[2], kv[3]);
-                *reinterpret_cast<float4*>(&s.v[t][lane * 4]) = make_float4(vv[0], vv[1], vv[2], vv[3]);
-                s.z[t][lane] = zraw;
-                if (lane == 0) {
-                    const float x = a_in + dtb;
-                    const float sp = x > kSoftplusThreshold ? x : log1pf(expf(x));
-                    s.decay[t] = expf(-expf(alog) * sp);
-                    s.beta[t] = 1.0f / (1.0f + expf(-b_in));
-                    s.kq[t] = kq;
-                    s.row[t] = r;
-                    s.ws[t] = ws;
-                }
-            }
-        }
+// Per-token prologue arithmetic for token t of unit (i, h), one warp: the raw
+// quads are this lane's 4 elements of q, k (key head), v and z (v-head);
+// `ws` is the slot that receives the state after this token (-1: none).
+__device__ __forceinline__ void prologue_token(Smem& s, const Params& p, int h, int t, int r, int lane,
+                                               uint2 qraw, uint2 kraw, uint2 vraw, uint2 zraw, long long ws) {
+    float a_in = 0.f, b_in = 0.f, dtb = 0.f, alog = 0.f;
+    if (lane == 0) {
+        a_in = __bfloat162float(p.a[r * p.a_stride + h]);
+        b_in = __bfloat162float(p.b[r * p.b_stride + h]);
+        dtb = __bfloat162float(p.dt_bias[h]);
+        alog = __ldg(p.A_log + h);
     }
-    // publishes the prologue; every CTA of the cluster checks every token row,
-    // so the skip decision below is the same in all of them
-    if (__syncthreads_or(bad)) { raise_flag(p, rank, GDN_FLAG_TOKEN_ROW); return; }
+    float qv[4], kv[4], vv[4];
+    unpack_bf16x4(qraw, qv);
+    unpack_bf16x4(kraw, kv);
+    unpack_bf16x4(vraw, vv);
+    float sq = 0.f, sk = 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) { sq += qv[e] * qv[e]; sk += kv[e] * kv[e]; }
+    sq = warp_sum(sq);
+    sk = warp_sum(sk);
+    const float rq = rsqrtf(sq + kQkEps) * p.scale;
+    const float rk = rsqrtf(sk + kQkEps);
+    float kq = 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) { qv[e] *= rq; kv[e] *= rk; kq += qv[e] * kv[e]; }
+    kq = warp_sum(kq);
+    *reinterpret_cast<float4*>(&s.q[t][kpos(lane * 4)]) = make_float4(qv[0], qv[1], qv[2], qv[3]);
+    *reinterpret_cast<float4*>(&s.k[t][kpos(lane * 4)]) = make_float4(kv[0], kv[1], kv[2], kv[3]);
+    *reinterpret_cast<float4*>(&s.v[t][lane * 4]) = make_float4(vv[0], vv[1], vv[2], vv[3]);
+    s.z[t][lane] = zraw;
+    if (lane == 0) {
+        const float x = a_in + dtb;
+        const float sp = x > kSoftplusThreshold ? x : log1pf(expf(x));
+        s.decay[t] = expf(-expf(alog) * sp);
+        s.beta[t] = 1.0f / (1.0f + expf(-b_in));
+        s.kq[t] = kq;
+        s.row[t] = r;
+        s.ws[t] = ws;
+    }
+}
 
-    // ---- the draft tokens, in order ----
-    StateT* pool = static_cast<StateT*>(p.pool);
+// One draft token for this lane's 16x4 block: both reductions, the delta rule,
+// the readout into s.o, the state update and (when s.ws[t] names a slot) the
+// slot write.
+template <typename StateT>
+__device__ __forceinline__ void token_step(float (&S)[kRowsPerLane][4], Smem& s, const Params& p, int t, int h,
+                                           int lane, int col0, int row0, int rank) {
+    const int cgi = lane & 3;
+    const int rg = lane >> 2;
     const int c_own = rg & 3;          // after the reduce-scatter: my column ...
     const int d_own = rg >> 2;         // ... and which dot product (0: k, 1: q)
-    for (int t = 0; t < q_len; ++t) {
-        const float decay = s.decay[t];
-        const float beta = s.beta[t];
-        const float kq = s.kq[t];
+    const float decay = s.decay[t];
+    const float beta = s.beta[t];
+    const float kq = s.kq[t];
 
-        // partial S^T k^ and S^T q^ over this lane's 16 rows, 4 columns each
-        float x[8];
+    // partial S^T k^ and S^T q^ over this lane's 16 rows, 4 columns each
+    float x[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) x[e] = 0.f;
+    for (int e = 0; e < 8; ++e) x[e] = 0.f;
 #pragma unroll
-        for (int r4 = 0; r4 < kRowsPerLane / 4; ++r4) {
-            const float4 kk = *reinterpret_cast<const float4*>(&s.k[t][kpos(row0 + 4 * r4)]);
-            const float4 qq = *reinterpret_cast<const float4*>(&s.q[t][kpos(row0 + 4 * r4)]);
-            const float kr[4] = {kk.x, kk.y, kk.z, kk.w};
-            const float qr[4] = {qq.x, qq.y, qq.z, qq.w};
+    for (int r4 = 0; r4 < kRowsPerLane / 4; ++r4) {
+        const float4 kk = *reinterpret_cast<const float4*>(&s.k[t][kpos(row0 + 4 * r4)]);
+        const float4 qq = *reinterpret_cast<const float4*>(&s.q[t][kpos(row0 + 4 * r4)]);
+        const float kr[4] = {kk.x, kk.y, kk.z, kk.w};
+        const float qr[4] = {qq.x, qq.y, qq.z, qq.w};
 #pragma unroll
-            for (int rr = 0; rr < 4; ++rr)
+        for (int rr = 0; rr < 4; ++rr)
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    x[c] = fmaf(S[4 * r4 + rr][c], kr[rr], x[c]);
-                    x[4 + c] = fmaf(S[4 * r4 + rr][c], qr[rr], x[4 + c]);
-                }
-        }
-        // reduce-scatter over the 8 row groups (lane bits 4, 3, 2): afterwards
-        // lane (cg, rg) holds the full sum of value index rg = 4 d + c
-        float y[4];
-        {
-            const bool hi = (lane >> 4) & 1;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float send = hi ? x[e] : x[4 + e];
-                const float keep = hi ? x[4 + e] : x[e];
-                y[e] = keep + __shfl_xor_sync(kFull, send, 16);
+            for (int c = 0; c < 4; ++c) {
+                x[c] = fmaf(S[4 * r4 + rr][c], kr[rr], x[c]);
+                x[4 + c] = fmaf(S[4 * r4 + rr][c], qr[rr], x[4 + c]);
             }
-        }
-        float z2[2];
-        {
-            const bool hi = (lane >> 3) & 1;
+    }
+    // reduce-scatter over the 8 row groups (lane bits 4, 3, 2): afterwards
+    // lane (cg, rg) holds the full sum of value index rg = 4 d + c
+    float y[4];
+    {
+        const bool hi = (lane >> 4) & 1;
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const float send = hi ? y[e] : y[2 + e];
-                const float keep = hi ? y[2 + e] : y[e];
-                z2[e] = keep + __shfl_xor_sync(kFull, send, 8);
-            }
-        }
-        float dot;
-        {
-            const bool hi = (lane >> 2) & 1;
-            const float send = hi ? z2[0] : z2[1];
-            const float keep = hi ? z2[1] : z2[0];
-            dot = keep + __shfl_xor_sync(kFull, send, 4);
-        }
-        // delta rule on the k lanes; readout on the q lanes
-        const float vp = beta * (s.v[t][col0 + c_own] - decay * dot);   // valid where d_own == 0
-        const float vp_pair = __shfl_xor_sync(kFull, vp, 16);
-        if (d_own == 1) s.o[t][col0 + c_own] = fmaf(decay, dot, kq * vp_pair);
-        float vpc[4];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) vpc[c] = __shfl_sync(kFull, vp, cgi + 4 * c);
-
-        // S <- e^g S + k^ v'^T
-#pragma unroll
-        for (int r4 = 0; r4 < kRowsPerLane / 4; ++r4) {
-            const float4 kk = *reinterpret_cast<const float4*>(&s.k[t][kpos(row0 + 4 * r4)]);
-            const float kr[4] = {kk.x, kk.y, kk.z, kk.w};
-#pragma unroll
-            for (int rr = 0; rr < 4; ++rr)
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    S[4 * r4 + rr][c] = fmaf(S[4 * r4 + rr][c], decay, kr[rr] * vpc[c]);
-        }
-
-        // the state after token t goes to slot state_indices[i, t] (skip -1)
-        const long long ws = s.ws[t];
-        const bool write = ws >= 0 && ws < p.num_slots;
-        if (ws >= p.num_slots) raise_flag(p, rank, GDN_FLAG_SLOT_RANGE);
-        StateT* dst = pool + (ws * p.H_v + h) * kTile;
-        if (write) {
-            StateT* d = dst + static_cast<int64_t>(row0) * kV + col0;
-#pragma unroll
-            for (int r = 0; r < kRowsPerLane; ++r) StateIO<StateT>::store4(d + r * kV, S[r]);
+        for (int e = 0; e < 4; ++e) {
+            const float send = hi ? x[e] : x[4 + e];
+            const float keep = hi ? x[4 + e] : x[e];
+            y[e] = keep + __shfl_xor_sync(kFull, send, 16);
         }
     }
+    float z2[2];
+    {
+        const bool hi = (lane >> 3) & 1;
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const float send = hi ? y[e] : y[2 + e];
+            const float keep = hi ? y[2 + e] : y[e];
+            z2[e] = keep + __shfl_xor_sync(kFull, send, 8);
+        }
+    }
+    float dot;
+    {
+        const bool hi = (lane >> 2) & 1;
+        const float send = hi ? z2[0] : z2[1];
+        const float keep = hi ? z2[1] : z2[0];
+        dot = keep + __shfl_xor_sync(kFull, send, 4);
+    }
+    // delta rule on the k lanes; readout on the q lanes
+    const float vp = beta * (s.v[t][col0 + c_own] - decay * dot);   // valid where d_own == 0
+    const float vp_pair = __shfl_xor_sync(kFull, vp, 16);
+    if (d_own == 1) s.o[t][col0 + c_own] = fmaf(decay, dot, kq * vp_pair);
+    float vpc[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) vpc[c] = __shfl_sync(kFull, vp, cgi + 4 * c);
 
-    // ---- gated RMSNorm epilogue ----
-    __syncthreads();                                           // s.o of this CTA complete
+    // S <- e^g S + k^ v'^T
+#pragma unroll
+    for (int r4 = 0; r4 < kRowsPerLane / 4; ++r4) {
+        const float4 kk = *reinterpret_cast<const float4*>(&s.k[t][kpos(row0 + 4 * r4)]);
+        const float kr[4] = {kk.x, kk.y, kk.z, kk.w};
+#pragma unroll
+        for (int rr = 0; rr < 4; ++rr)
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+                S[4 * r4 + rr][c] = fmaf(S[4 * r4 + rr][c], decay, kr[rr] * vpc[c]);
+    }
+
+    // the state after token t goes to slot s.ws[t] (skip -1)
+    const long long ws = s.ws[t];
+    if (ws >= p.num_slots) raise_flag(p, rank, GDN_FLAG_SLOT_RANGE);
+    if (ws >= 0 && ws < p.num_slots) {
+        StateT* d = static_cast<StateT*>(p.pool) + (ws * p.H_v + h) * kTile + static_cast<int64_t>(row0) * kV + col0;
+#pragma unroll
+        for (int r = 0; r < kRowsPerLane; ++r) StateIO<StateT>::store4(d + r * kV, S[r]);
+    }
+}
+
+// Gated RMSNorm epilogue over tokens 0 .. n-1 in shared memory: out = o *
+// rsqrt(mean(o^2) + eps) * w * silu(z), written at the rows in s.row.  With
+// SPLIT > 1 the mean-square is combined across the cluster through
+// distributed shared memory.
+template <int SPLIT>
+__device__ __forceinline__ void epilogue(Smem& s, const Params& p, int h, int n, int warp, int lane, int rank) {
+    constexpr int W = 8 / SPLIT;
+    constexpr int CW = kV / SPLIT;  // V columns of this CTA
+    const bool gated = p.z != nullptr;
     if (SPLIT > 1 && gated) {
-        // partial mean-square numerators over this CTA's columns, combined
-        // across the cluster through distributed shared memory
-        for (int t = warp; t < q_len; t += W) {
+        for (int t = warp; t < n; t += W) {
             float ss = 0.f;
             for (int c = lane; c < CW; c += 32) {
                 const float o = s.o[t][rank * CW + c];
@@ -399,7 +342,7 @@ gdn_spec_decode_kernel(const Params p) {
         }
         cg::this_cluster().sync();
     }
-    for (int t = warp; t < q_len; t += W) {
+    for (int t = warp; t < n; t += W) {
         float rinv = 1.0f;
         if (gated) {
             float ss = 0.f;
@@ -435,6 +378,171 @@ gdn_spec_decode_kernel(const Params p) {
         }
     }
     if (SPLIT > 1 && gated) cg::this_cluster().sync();         // peers may still read s.red
+}
+
+// this lane's 4 elements of token row r: q, k (key head kh), v, z (v-head h)
+__device__ __forceinline__ void load_token_quads(const Params& p, int r, int kh, int h, int lane, uint2& qraw,
+                                                 uint2& kraw, uint2& vraw, uint2& zraw) {
+    qraw = ldg_quad(p.q + r * p.q_stride + kh * kK + lane * 4);
+    kraw = ldg_quad(p.k + r * p.k_stride + kh * kK + lane * 4);
+    vraw = ldg_quad(p.v + r * p.v_stride + static_cast<int64_t>(h) * kV + lane * 4);
+    zraw = p.z != nullptr ? ldg_quad(p.z + r * p.z_stride + static_cast<int64_t>(h) * kV + lane * 4)
+                          : make_uint2(0, 0);
+}
+
+// ---- the speculative decode kernel -------------------------------------------------
+//
+// Grid: one CTA per (unit, column slice); SPLIT CTAs of a unit form one cluster.
+// Block: 8 / SPLIT warps, each owning 16 of the unit's 128 V columns.
+template <typename StateT, int SPLIT>
+__global__ void __launch_bounds__(Config<StateT, SPLIT>::kThreads, 2 * SPLIT)
+gdn_spec_decode_kernel(const Params p) {
+    using C = Config<StateT, SPLIT>;
+    constexpr int W = C::kWarps;
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    Smem& s = *reinterpret_cast<Smem*>(smem_raw);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int rank = SPLIT > 1 ? static_cast<int>(blockIdx.x % SPLIT) : 0;
+    const int unit = static_cast<int>(blockIdx.x / SPLIT);
+    const int i = unit / p.H_v;
+    const int h = unit - i * p.H_v;
+    const int cgi = lane & 3;        // column group: 4 consecutive columns
+    const int rg = lane >> 2;        // row group: 16 consecutive K rows
+    const int wg = rank * W + warp;  // this warp's 16-column block (0..7)
+    const int col0 = wg * kColsPerWarp + cgi * 4;
+    const int row0 = rg * kRowsPerLane;
+
+    // ---- resolve the work item (every thread computes the same answer) ----
+    // The sequence's slot row is read in the same round trip as its length and
+    // acceptance, so the read slot costs no extra dependent load.
+    const int32_t* slot_row = p.idx + static_cast<int64_t>(i) * p.stride;
+    int slots[kMaxT];
+#pragma unroll
+    for (int j = 0; j < kMaxT; ++j) slots[j] = j < p.stride ? __ldg(slot_row + j) : -1;
+    const int bos = __ldg(p.cu + i);
+    const int q_len = __ldg(p.cu + i + 1) - bos;
+    const int acc = __ldg(p.num_acc + i);
+    if (q_len <= 0) return;                                    // nothing to do
+    // token positions must lie inside [0, cu_seqlens[batch]), the length of
+    // spec_token_indx (rows themselves are range-checked below)
+    if (bos < 0 || bos + q_len > __ldg(p.cu + p.batch)) { raise_flag(p, rank, GDN_FLAG_TOKEN_ROW); return; }
+    if (acc > p.stride) { raise_flag(p, rank, GDN_FLAG_ACCEPTED); return; }
+    if (q_len > p.max_T || q_len > p.stride) { raise_flag(p, rank, GDN_FLAG_QLEN); return; }
+    // rewind: the state after the last accepted token; acc-1 clamped at 0
+    const int rj = max(acc - 1, 0);
+    long long rs = 0;
+#pragma unroll
+    for (int j = 0; j < kMaxT; ++j)
+        if (j == rj) rs = slots[j];
+    if (rj >= kMaxT) rs = __ldg(slot_row + rj);                // acceptance beyond the first 8 columns
+    if (rs < 0) return;                                        // padded sequence
+    if (rs >= p.num_slots) { raise_flag(p, rank, GDN_FLAG_SLOT_RANGE); return; }
+
+    // ---- load this lane's 16x4 block of the state tile (FP32 in registers) ----
+    const StateT* src = static_cast<const StateT*>(p.pool) + (rs * p.H_v + h) * kTile;
+    float S[kRowsPerLane][4];
+#pragma unroll
+    for (int r = 0; r < kRowsPerLane; ++r)
+        StateIO<StateT>::load4(src + static_cast<int64_t>(row0 + r) * kV + col0, S[r]);
+
+    // ---- per-token prologue: gather rows, gates, normalised q / k, v, z ----
+    const int kh = h / p.group;
+    if (p.z != nullptr && warp == 0) s.w[lane] = ldg_quad(p.norm_w + lane * 4);
+    int bad = 0;
+#pragma unroll
+    for (int j = 0; j < SPLIT; ++j) {                          // W * SPLIT = 8 >= q_len
+        const int t = warp + j * W;
+        if (t < q_len) {
+            const int n = bos + t;
+            const int r = p.sti != nullptr ? __ldg(p.sti + n) : n;
+            if (r < 0 || r >= p.num_tokens) {
+                bad = 1;
+            } else {
+                uint2 qraw, kraw, vraw, zraw;
+                load_token_quads(p, r, kh, h, lane, qraw, kraw, vraw, zraw);
+                long long ws = 0;
+#pragma unroll
+                for (int jj = 0; jj < kMaxT; ++jj)
+                    if (jj == t) ws = slots[jj];                   // t < q_len <= 8
+                prologue_token(s, p, h, t, r, lane, qraw, kraw, vraw, zraw, ws);
+            }
+        }
+    }
+    // publishes the prologue; every CTA of the cluster checks every token row,
+    // so the skip decision below is the same in all of them
+    if (__syncthreads_or(bad)) { raise_flag(p, rank, GDN_FLAG_TOKEN_ROW); return; }
+
+    // ---- the draft tokens, in order ----
+    for (int t = 0; t < q_len; ++t) token_step<StateT>(S, s, p, t, h, lane, col0, row0, rank);
+
+    // ---- gated RMSNorm epilogue ----
+    __syncthreads();                                           // s.o of this CTA complete
+    epilogue<SPLIT>(s, p, h, q_len, warp, lane, rank);
+}
+
+// ---- the prefill kernel (recurrent form) -------------------------------------------
+//
+// One CTA of 8 warps per (sequence, v-head): the prompt runs through the same
+// per-token step as the decode path, 8 tokens per round of prologue / tokens /
+// epilogue, with the FP32 state in registers from the first token to the
+// last; only the final state is stored.
+template <typename StateT>
+__global__ void __launch_bounds__(256, 2) gdn_prefill_kernel(const Params p) {
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    Smem& s = *reinterpret_cast<Smem*>(smem_raw);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int unit = static_cast<int>(blockIdx.x);
+    const int i = unit / p.H_v;
+    const int h = unit - i * p.H_v;
+    const int cgi = lane & 3;
+    const int rg = lane >> 2;
+    const int col0 = warp * kColsPerWarp + cgi * 4;
+    const int row0 = rg * kRowsPerLane;
+
+    const int bos = __ldg(p.cu + i);
+    const int L = __ldg(p.cu + i + 1) - bos;
+    const long long rs = __ldg(p.read_slots + i);
+    const long long wsl = __ldg(p.write_slots + i);
+    if (L <= 0) return;
+    if (bos < 0 || bos + L > p.num_tokens) { raise_flag(p, 0, GDN_FLAG_TOKEN_ROW); return; }
+    if (rs >= p.num_slots || wsl >= p.num_slots) { raise_flag(p, 0, GDN_FLAG_SLOT_RANGE); return; }
+
+    float S[kRowsPerLane][4];
+    if (rs >= 0) {
+        const StateT* src = static_cast<const StateT*>(p.pool) + (rs * p.H_v + h) * kTile;
+#pragma unroll
+        for (int r = 0; r < kRowsPerLane; ++r)
+            StateIO<StateT>::load4(src + static_cast<int64_t>(row0 + r) * kV + col0, S[r]);
+    } else {
+#pragma unroll
+        for (int r = 0; r < kRowsPerLane; ++r)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) S[r][c] = 0.f;         // no initial state
+    }
+    const int kh = h / p.group;
+    if (p.z != nullptr && warp == 0) s.w[lane] = ldg_quad(p.norm_w + lane * 4);
+    for (int c0 = 0; c0 < L; c0 += kMaxT) {
+        const int n = min(kMaxT, L - c0);
+        if (warp < n) {
+            const int r = bos + c0 + warp;
+            uint2 qraw, kraw, vraw, zraw;
+            load_token_quads(p, r, kh, h, lane, qraw, kraw, vraw, zraw);
+            prologue_token(s, p, h, warp, r, lane, qraw, kraw, vraw, zraw, -1);
+        }
+        __syncthreads();                                       // prologue published
+        for (int t = 0; t < n; ++t) token_step<StateT>(S, s, p, t, h, lane, col0, row0, 0);
+        __syncthreads();                                       // s.o complete
+        epilogue<1>(s, p, h, n, warp, lane, 0);
+        __syncthreads();                                       // before the next round overwrites s
+    }
+    if (wsl >= 0) {
+        StateT* d = static_cast<StateT*>(p.pool) + (wsl * p.H_v + h) * kTile + static_cast<int64_t>(row0) * kV + col0;
+#pragma unroll
+        for (int r = 0; r < kRowsPerLane; ++r) StateIO<StateT>::store4(d + r * kV, S[r]);
+    }
 }
 
 // ---- host side ----------------------------------------------------------------
@@ -484,6 +592,17 @@ cudaError_t launch_split(const Params& p, int64_t units, int split, cudaStream_t
     }
 }
 
+template <typename StateT>
+cudaError_t launch_prefill(const Params& p, int64_t units, cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(units), 1, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.dynamicSmemBytes = sizeof(Smem);
+    cfg.stream = stream;
+    cfg.numAttrs = 0;
+    return cudaLaunchKernelEx(&cfg, gdn_prefill_kernel<StateT>, p);
+}
+
 bool aligned(const void* ptr, uintptr_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }
 
 // One CTA per unit at every batch size measured (4 to 128 sequences of 16
@@ -507,28 +626,31 @@ gdn_status check_dims(const gdn_dims* d) {
     return GDN_OK;
 }
 
-}  // namespace
+// Sizes shared by both entry points (decode-only fields are not checked here).
+gdn_status check_common_dims(const gdn_dims* d) {
+    if (d == nullptr) return GDN_ERR_NULL_ARG;
+    if (d->batch < 0 || d->num_tokens < 0 || d->H_k <= 0 || d->H_v <= 0 || d->num_slots < 1 ||
+        d->H_v % d->H_k != 0 || d->reserved != 0)
+        return GDN_ERR_BAD_SHAPE;
+    if (d->q_stride < 0 || d->k_stride < 0 || d->v_stride < 0 || d->a_stride < 0 || d->b_stride < 0 ||
+        d->z_stride < 0 || d->out_stride < 0)
+        return GDN_ERR_BAD_SHAPE;
+    if (d->K != kK || d->V != kV) return GDN_ERR_UNSUPPORTED;
+    if (static_cast<int64_t>(d->batch) * d->H_v * 8 > 0x7fffffffLL) return GDN_ERR_BAD_SHAPE;
+    return GDN_OK;
+}
 
-extern "C" {
-
-gdn_status gdn_spec_decode(const void* q, const void* k, const void* v, const void* a, const void* b,
-                           const void* z, const float* A_log, const void* dt_bias, const void* norm_w,
-                           void* state_pool, const int32_t* state_indices, const int32_t* num_accepted,
-                           const int32_t* cu_seqlens, const int32_t* spec_token_indx, void* out,
-                           const gdn_dims* dims, float scale, float eps, gdn_dtype state_dtype,
-                           int32_t* status_word, gdn_stream_t stream) {
-    const gdn_status ds = check_dims(dims);
-    if (ds != GDN_OK) return ds;
-    if (state_dtype != GDN_F32 && state_dtype != GDN_BF16 && state_dtype != GDN_F16) return GDN_ERR_UNSUPPORTED;
-    if (dims->batch == 0) return GDN_OK;
-    if (!q || !k || !v || !a || !b || !A_log || !dt_bias || !state_pool || !state_indices || !num_accepted ||
-        !cu_seqlens || !out)
+// Fill the kernel parameters from the call and check pointers and alignment.
+gdn_status make_params(Params& p, const void* q, const void* k, const void* v, const void* a, const void* b,
+                       const void* z, const float* A_log, const void* dt_bias, const void* norm_w, void* state_pool,
+                       const int32_t* cu_seqlens, void* out, const gdn_dims* dims, float scale, float eps,
+                       int32_t* status_word) {
+    if (!q || !k || !v || !a || !b || !A_log || !dt_bias || !state_pool || !cu_seqlens || !out)
         return GDN_ERR_NULL_ARG;
     if ((z == nullptr) != (norm_w == nullptr)) return GDN_ERR_NULL_ARG;
-
     const int64_t qk_row = static_cast<int64_t>(dims->H_k) * kK;
     const int64_t v_row = static_cast<int64_t>(dims->H_v) * kV;
-    Params p;
+    p = Params{};
     p.q = static_cast<const __nv_bfloat16*>(q);
     p.k = static_cast<const __nv_bfloat16*>(k);
     p.v = static_cast<const __nv_bfloat16*>(v);
@@ -539,10 +661,7 @@ gdn_status gdn_spec_decode(const void* q, const void* k, const void* v, const vo
     p.dt_bias = static_cast<const __nv_bfloat16*>(dt_bias);
     p.norm_w = static_cast<const __nv_bfloat16*>(norm_w);
     p.pool = state_pool;
-    p.idx = state_indices;
-    p.num_acc = num_accepted;
     p.cu = cu_seqlens;
-    p.sti = spec_token_indx;
     p.out = static_cast<__nv_bfloat16*>(out);
     p.status = status_word;
     p.q_stride = dims->q_stride ? dims->q_stride : qk_row;
@@ -562,26 +681,89 @@ gdn_status gdn_spec_decode(const void* q, const void* k, const void* v, const vo
     p.group = dims->H_v / dims->H_k;
     p.scale = scale;
     p.eps = eps;
-
     // vector accesses: 16 B state rows, 8 B bf16 quads
     if (!aligned(state_pool, 16) || !aligned(q, 8) || !aligned(k, 8) || !aligned(v, 8) || !aligned(out, 8) ||
         (z && !aligned(z, 8)) || (norm_w && !aligned(norm_w, 8)) || !aligned(a, 2) || !aligned(b, 2) ||
-        !aligned(dt_bias, 2) || !aligned(A_log, 4) || !aligned(state_indices, 4) || !aligned(num_accepted, 4) ||
-        !aligned(cu_seqlens, 4) || (spec_token_indx && !aligned(spec_token_indx, 4)) ||
+        !aligned(dt_bias, 2) || !aligned(A_log, 4) || !aligned(cu_seqlens, 4) ||
         (status_word && !aligned(status_word, 4)))
         return GDN_ERR_MISALIGNED;
     if (p.q_stride % 4 || p.k_stride % 4 || p.v_stride % 4 || p.z_stride % 4 || p.out_stride % 4)
         return GDN_ERR_MISALIGNED;
+    return GDN_OK;
+}
 
+template <template <typename> class Launcher, typename... Args>
+cudaError_t by_state_dtype(gdn_dtype dt, Args... args) {
+    switch (dt) {
+    case GDN_F32: return Launcher<float>::run(args...);
+    case GDN_BF16: return Launcher<__nv_bfloat16>::run(args...);
+    default: return Launcher<__half>::run(args...);
+    }
+}
+
+template <typename StateT>
+struct DecodeLauncher {
+    static cudaError_t run(const Params& p, int64_t units, int split, cudaStream_t s) {
+        return launch_split<StateT>(p, units, split, s);
+    }
+};
+
+template <typename StateT>
+struct PrefillLauncher {
+    static cudaError_t run(const Params& p, int64_t units, cudaStream_t s) { return launch_prefill<StateT>(p, units, s); }
+};
+
+}  // namespace
+
+extern "C" {
+
+gdn_status gdn_spec_decode(const void* q, const void* k, const void* v, const void* a, const void* b,
+                           const void* z, const float* A_log, const void* dt_bias, const void* norm_w,
+                           void* state_pool, const int32_t* state_indices, const int32_t* num_accepted,
+                           const int32_t* cu_seqlens, const int32_t* spec_token_indx, void* out,
+                           const gdn_dims* dims, float scale, float eps, gdn_dtype state_dtype,
+                           int32_t* status_word, gdn_stream_t stream) {
+    const gdn_status ds = check_dims(dims);
+    if (ds != GDN_OK) return ds;
+    if (state_dtype != GDN_F32 && state_dtype != GDN_BF16 && state_dtype != GDN_F16) return GDN_ERR_UNSUPPORTED;
+    if (dims->batch == 0) return GDN_OK;
+    if (!state_indices || !num_accepted) return GDN_ERR_NULL_ARG;
+    Params p;
+    const gdn_status ps = make_params(p, q, k, v, a, b, z, A_log, dt_bias, norm_w, state_pool, cu_seqlens, out,
+                                      dims, scale, eps, status_word);
+    if (ps != GDN_OK) return ps;
+    if (!aligned(state_indices, 4) || !aligned(num_accepted, 4) || (spec_token_indx && !aligned(spec_token_indx, 4)))
+        return GDN_ERR_MISALIGNED;
+    p.idx = state_indices;
+    p.num_acc = num_accepted;
+    p.sti = spec_token_indx;
     const int64_t units = static_cast<int64_t>(dims->batch) * dims->H_v;
     const int split = dims->split ? dims->split : choose_split(units);
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    cudaError_t err;
-    switch (state_dtype) {
-    case GDN_F32: err = launch_split<float>(p, units, split, s); break;
-    case GDN_BF16: err = launch_split<__nv_bfloat16>(p, units, split, s); break;
-    default: err = launch_split<__half>(p, units, split, s); break;
-    }
+    const cudaError_t err =
+        by_state_dtype<DecodeLauncher>(state_dtype, p, units, split, reinterpret_cast<cudaStream_t>(stream));
+    return err == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+gdn_status gdn_prefill(const void* q, const void* k, const void* v, const void* a, const void* b, const void* z,
+                       const float* A_log, const void* dt_bias, const void* norm_w, void* state_pool,
+                       const int32_t* read_slots, const int32_t* write_slots, const int32_t* cu_seqlens, void* out,
+                       const gdn_dims* dims, float scale, float eps, gdn_dtype state_dtype, int32_t* status_word,
+                       gdn_stream_t stream) {
+    const gdn_status ds = check_common_dims(dims);
+    if (ds != GDN_OK) return ds;
+    if (state_dtype != GDN_F32 && state_dtype != GDN_BF16 && state_dtype != GDN_F16) return GDN_ERR_UNSUPPORTED;
+    if (dims->batch == 0) return GDN_OK;
+    if (!read_slots || !write_slots) return GDN_ERR_NULL_ARG;
+    Params p;
+    const gdn_status ps = make_params(p, q, k, v, a, b, z, A_log, dt_bias, norm_w, state_pool, cu_seqlens, out,
+                                      dims, scale, eps, status_word);
+    if (ps != GDN_OK) return ps;
+    if (!aligned(read_slots, 4) || !aligned(write_slots, 4)) return GDN_ERR_MISALIGNED;
+    p.read_slots = read_slots;
+    p.write_slots = write_slots;
+    const int64_t units = static_cast<int64_t>(dims->batch) * dims->H_v;
+    const cudaError_t err =
+        by_state_dtype<PrefillLauncher>(state_dtype, p, units, reinterpret_cast<cudaStream_t>(stream));
     return err == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 

@@ -156,6 +156,40 @@ GDNSPEC_API gdn_status gdn_spec_decode(
     int32_t* status_word, gdn_stream_t stream);
 
 /*
+ * gdn_prefill -- the same gated delta rule over whole prompts: the prefill
+ * path whose state is carried across the prompt and written back to its slot
+ * ("PR #52191 report -- [CPU] Support FP16/BF16 persisted GDN state on AMX",
+ * implementation steps 3-4: arithmetic in FP32, the slot written in the pool
+ * dtype, rounded once).
+ *
+ * Sequence i is token rows cu_seqlens[i] .. cu_seqlens[i+1]-1, in order (no
+ * gather).  It starts from slot read_slots[i], or from the zero state when
+ * read_slots[i] < 0; every token writes its output row (with the gated RMSNorm
+ * epilogue when z / norm_w are given); the state after its last token goes to
+ * slot write_slots[i] (no write when negative).  read_slots[i] ==
+ * write_slots[i] updates a slot in place.
+ *
+ *   read_slots, write_slots   int32 [batch] (device)
+ *   every other argument       as for gdn_spec_decode; dims->spec_stride,
+ *                              max_T and split are not used
+ *
+ * Caller contract: non-negative write slots are distinct; no sequence reads a
+ * slot that another sequence writes.  Bad device data skips the sequence:
+ * a slot >= num_slots sets GDN_FLAG_SLOT_RANGE, rows outside [0, num_tokens)
+ * set GDN_FLAG_TOKEN_ROW.  Asynchronous on `stream`, allocates nothing.
+ */
+GDNSPEC_API gdn_status gdn_prefill(
+    const void* q, const void* k, const void* v,
+    const void* a, const void* b, const void* z,
+    const float* A_log, const void* dt_bias, const void* norm_w,
+    void* state_pool,
+    const int32_t* read_slots, const int32_t* write_slots,
+    const int32_t* cu_seqlens,
+    void* out,
+    const gdn_dims* dims, float scale, float eps, gdn_dtype state_dtype,
+    int32_t* status_word, gdn_stream_t stream);
+
+/*
  * The CTAs per (sequence, v-head) that gdn_spec_decode would use for these
  * sizes when dims->split == 0 (1, 2, 4 or 8), or 0 for invalid dims.  Host
  * only; queries the current device's SM count.

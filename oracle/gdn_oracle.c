@@ -510,4 +510,81 @@ int gdn_oracle_decode_nonspec(const gdn_oracle_problem* p)
     return ORC_OK;
 }
 
+/*
+ * Prefill over whole prompts (PR #52191 report, implementation step 3: the
+ * chunked prefill kernel chunk_gated_delta_rule_fwd_inter_kernel_impl carries
+ * the state across the prompt in FP32 and writes it back to its slot).
+ * Sequence i is tokens cu_seqlens[i] .. cu_seqlens[i+1]-1 (rows in order, no
+ * gather).  It starts from slot read_slots[i], or from the zero state when
+ * read_slots[i] < 0, runs the same per-token step as the decode path over all
+ * of its tokens in order, writes one output row per token, and stores the
+ * state after its last token in slot write_slots[i] (skipped when negative),
+ * rounded once.  Reading: the pages' CPU chunk kernel also rounds a narrow
+ * state at every chunk write-back; here, as on the decode path, only the
+ * stored copy is rounded and the carried state stays wide.
+ * `p->state_indices`, `num_accepted` and `spec_token_indx` are ignored.
+ */
+int gdn_oracle_prefill(const gdn_oracle_problem* p, const int32_t* read_slots, const int32_t* write_slots)
+{
+    if (!p || !p->q || !p->k || !p->v || !p->a || !p->b || !p->A_log || !p->dt_bias || !p->pool ||
+        !p->cu_seqlens || !read_slots || !write_slots)
+        return ORC_ERR_NULL;
+    if ((p->z == NULL) != (p->norm_w == NULL)) return ORC_ERR_NULL;
+    if (p->batch < 0 || p->H_k <= 0 || p->H_v <= 0 || p->H_v % p->H_k != 0 || p->num_slots <= 0)
+        return ORC_ERR_SHAPE;
+    const int64_t K = p->K, V = p->V, H_v = p->H_v;
+    /* contract: rows in range, write slots distinct, no read slot written by
+       another sequence */
+    for (int64_t i = 0; i < p->batch; ++i) {
+        if (p->cu_seqlens[i] < 0 || p->cu_seqlens[i + 1] > p->num_tokens) return ORC_ERR_ROW;
+        if (read_slots[i] >= p->num_slots || write_slots[i] >= p->num_slots) return ORC_ERR_SLOT;
+        for (int64_t j = 0; j < p->batch; ++j) {
+            if (j != i && write_slots[j] >= 0 &&
+                (write_slots[j] == write_slots[i] || write_slots[j] == read_slots[i]))
+                return ORC_ERR_CONFLICT;
+        }
+    }
+    const int64_t work_len = K * V + 2 * K + V;
+    const int nthreads = p->num_threads > 0 ? p->num_threads : 1;
+    double* work_all = (double*)malloc(sizeof(double) * (size_t)(work_len * nthreads));
+    if (!work_all) return ORC_ERR_NOMEM;
+    const int64_t units = p->batch * H_v;
+#ifdef _OPENMP
+#pragma omp parallel for num_threads(nthreads) schedule(dynamic, 1)
+#endif
+    for (int64_t u = 0; u < units; ++u) {
+        const int64_t i = u / H_v, h = u % H_v;
+        int tid = 0;
+#ifdef _OPENMP
+        tid = omp_get_thread_num();
+#endif
+        double* S = work_all + (int64_t)tid * work_len;
+        double* kn = S + K * V;
+        double* qn = kn + K;
+        double* o = qn + K;
+        const int64_t bos = p->cu_seqlens[i], eos = p->cu_seqlens[i + 1];
+        if (eos <= bos) continue;
+        {
+            if (read_slots[i] >= 0) {
+                const int64_t src = ((int64_t)read_slots[i] * H_v + h) * K * V;
+                for (int64_t e = 0; e < K * V; ++e) S[e] = pool_get(p, src + e);
+            } else {
+                for (int64_t e = 0; e < K * V; ++e) S[e] = 0.0;
+            }
+            for (int64_t r = bos; r < eos; ++r) {
+                token_step(p, r, h, S, kn, qn, o);
+                epilogue(p, r, h, o);
+            }
+            if (write_slots[i] >= 0) {
+                const int64_t dst = ((int64_t)write_slots[i] * H_v + h) * K * V;
+                for (int64_t e = 0; e < K * V; ++e) pool_put(p, dst + e, S[e]);
+            }
+            if (p->states_f64 && p->states_T > 0)
+                memcpy(p->states_f64 + (i * H_v + h) * p->states_T * K * V, S, sizeof(double) * (size_t)(K * V));
+        }
+    }
+    free(work_all);
+    return ORC_OK;
+}
+
 int gdn_oracle_abi_version(void) { return 1; }

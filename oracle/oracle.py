@@ -82,6 +82,8 @@ def load() -> ctypes.CDLL:
             lib.gdn_oracle_spec_decode.restype = ctypes.c_int
             lib.gdn_oracle_decode_nonspec.argtypes = [ctypes.POINTER(Problem)]
             lib.gdn_oracle_decode_nonspec.restype = ctypes.c_int
+            lib.gdn_oracle_prefill.argtypes = [ctypes.POINTER(Problem), ctypes.c_void_p, ctypes.c_void_p]
+            lib.gdn_oracle_prefill.restype = ctypes.c_int
             for name in ("gdn_oracle_round_bf16", "gdn_oracle_round_f16", "gdn_oracle_round_f32",
                          "gdn_oracle_value_bf16", "gdn_oracle_value_f16"):
                 getattr(lib, name).argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64]
@@ -177,6 +179,43 @@ def decode_nonspec(*, q, k, v, a, b, z, A_log, dt_bias, norm_w, pool, state_dtyp
     if rc != 0:
         raise OracleError(f"oracle rejected the problem: {ERRORS.get(rc, rc)}")
     return {"out_f64": out_f64, "out_bf16": out_bf16}
+
+
+def prefill(*, q, k, v, a, b, z, A_log, dt_bias, norm_w, pool, state_dtype, cu_seqlens,
+            read_slots, write_slots, scale=128 ** -0.5, eps=1e-5, qk_eps=1e-6,
+            softplus_threshold=20.0, final_states=False, num_threads=1):
+    """Prefill over whole prompts: sequence i is rows cu_seqlens[i] ..
+    cu_seqlens[i+1]-1, starts from slot read_slots[i] (zero state when < 0)
+    and stores its final state in write_slots[i] (skipped when < 0).
+    ``pool`` is updated in place.  Returns out_f64 / out_bf16 and, with
+    final_states, the FP64 final state [batch, H_v, K, V]."""
+    lib = load()
+    q = _c(q, np.uint16); k = _c(k, np.uint16); v = _c(v, np.uint16)
+    a = _c(a, np.uint16); b = _c(b, np.uint16); z = _c(z, np.uint16)
+    A_log = _c(A_log, np.float32); dt_bias = _c(dt_bias, np.uint16); norm_w = _c(norm_w, np.uint16)
+    cu = _c(cu_seqlens, np.int32)
+    rd = _c(read_slots, np.int32); wr = _c(write_slots, np.int32)
+    N, H_k, K = q.shape
+    H_v, V = v.shape[1], v.shape[2]
+    batch = rd.shape[0]
+    out_f64 = np.full((N, H_v, V), np.nan)
+    out_bf16 = np.full((N, H_v, V), 0xFFFF, dtype=np.uint16)
+    states = np.full((batch, H_v, 1, K, V), np.nan) if final_states else None
+    p = Problem(
+        batch=batch, num_tokens=N, H_k=H_k, H_v=H_v, K=K, V=V, spec_stride=1,
+        num_slots=pool.shape[0], state_dtype=state_dtype, num_threads=num_threads,
+        scale=scale, eps=eps, qk_eps=qk_eps, softplus_threshold=softplus_threshold,
+        q=_ptr(q), k=_ptr(k), v=_ptr(v), a=_ptr(a), b=_ptr(b), z=_ptr(z),
+        A_log=_ptr(A_log), dt_bias=_ptr(dt_bias), norm_w=_ptr(norm_w),
+        cu_seqlens=_ptr(cu), pool=pool.ctypes.data,
+        out_f64=out_f64.ctypes.data, out_bf16=out_bf16.ctypes.data,
+        states_f64=_ptr(states), states_T=1 if final_states else 0,
+    )
+    rc = lib.gdn_oracle_prefill(ctypes.byref(p), rd.ctypes.data, wr.ctypes.data)
+    if rc != 0:
+        raise OracleError(f"oracle rejected the problem: {ERRORS.get(rc, rc)}")
+    return {"out_f64": out_f64, "out_bf16": out_bf16,
+            "states": None if states is None else states[:, :, 0]}
 
 
 def _unary(name, x, in_dtype, out_dtype):
