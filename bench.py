@@ -501,10 +501,12 @@ def run_prefill(args, rank, world, local_rank):
     pairs = [(torch.from_numpy(perm[2 * s * B:(2 * s + 1) * B].copy()).to(dev),
               torch.from_numpy(perm[(2 * s + 1) * B:(2 * s + 2) * B].copy()).to(dev)) for s in range(N_SETS)]
 
+    fn = gdn.gdn_prefill_chunked if args.prefill_form == "chunked" else gdn.gdn_prefill
+
     def step(s, stream=None):
         rd, wr = pairs[s % N_SETS]
-        gdn.gdn_prefill(t["q"], t["k"], t["v"], t["a"], t["b"], t["z"], t["A_log"], t["dt_bias"], t["norm_w"],
-                        pool, rd, wr, t["cu"], t["out"], stream=stream)
+        fn(t["q"], t["k"], t["v"], t["a"], t["b"], t["z"], t["A_log"], t["dt_bias"], t["norm_w"],
+           pool, rd, wr, t["cu"], t["out"], stream=stream)
 
     stream = torch.cuda.current_stream(dev)
     for s in range(max(args.warmup, 3)):
@@ -531,7 +533,8 @@ def run_prefill(args, rank, world, local_rank):
         "unit": "token·head updates/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
-        "config": {"workload": f"{args.workload}: {WORKLOADS[args.workload][0]}", "global_batch": B * world,
+        "config": {"workload": f"{args.workload}: {WORKLOADS[args.workload][0]}", "form": args.prefill_form,
+                   "global_batch": B * world,
                    "seq_len": int(case.q_lens().max()), "parallelism": f"independent batches, {world} GPU(s)"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": None, "peak_kind": f"{peak_kind} HBM copy bandwidth",
@@ -546,6 +549,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="bs32_t8_bf16")
+    ap.add_argument("--prefill-form", choices=("chunked", "recurrent"), default="chunked",
+                    help="prefill workloads: gdn_prefill_chunked (tensor cores) or gdn_prefill (per token)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

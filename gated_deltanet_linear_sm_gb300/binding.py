@@ -21,6 +21,7 @@ GDN_FLAG_SLOT_RANGE = 1
 GDN_FLAG_ACCEPTED = 2
 GDN_FLAG_QLEN = 4
 GDN_FLAG_TOKEN_ROW = 8
+GDN_FLAG_TIMEOUT = 16
 
 
 class gdn_dims(ctypes.Structure):
@@ -59,6 +60,8 @@ EXPORTS = {
                                                    ctypes.c_int, _VP, _VP]),
     "gdn_prefill": (ctypes.c_int, [_VP] * 14 + [ctypes.POINTER(gdn_dims), ctypes.c_float, ctypes.c_float,
                                                ctypes.c_int, _VP, _VP]),
+    "gdn_prefill_chunked": (ctypes.c_int, [_VP] * 14 + [ctypes.POINTER(gdn_dims), ctypes.c_float,
+                                                       ctypes.c_float, ctypes.c_int, _VP, _VP]),
     "gdn_spec_decode_split": (ctypes.c_int32, [ctypes.POINTER(gdn_dims)]),
     "gdn_status_str": (ctypes.c_char_p, [ctypes.c_int]),
     "gdn_version": (ctypes.c_int32, []),
@@ -255,9 +258,24 @@ def gdn_prefill(q, k, v, a, b, z, A_log, dt_bias, norm_w, state_pool, read_slots
     read_slots[i] (zero state when < 0) and stores its final state in slot
     write_slots[i] (none when < 0).  Tensors as for gdn_spec_decode;
     read_slots, write_slots [B] int32.  Returns ``out``."""
+    return _prefill("gdn_prefill", q, k, v, a, b, z, A_log, dt_bias, norm_w, state_pool, read_slots,
+                    write_slots, cu_seqlens, out, scale, eps, status, stream)
+
+
+def gdn_prefill_chunked(q, k, v, a, b, z, A_log, dt_bias, norm_w, state_pool, read_slots, write_slots,
+                        cu_seqlens, out, *, scale=128 ** -0.5, eps=1e-5, status=None, stream=None):
+    """The same prefill as gdn_prefill, computed chunk by chunk on the tensor
+    cores (bf16 operands, FP32 accumulation; see include/gdnspec.h).  Same
+    arguments; returns ``out``."""
+    return _prefill("gdn_prefill_chunked", q, k, v, a, b, z, A_log, dt_bias, norm_w, state_pool, read_slots,
+                    write_slots, cu_seqlens, out, scale, eps, status, stream)
+
+
+def _prefill(entry, q, k, v, a, b, z, A_log, dt_bias, norm_w, state_pool, read_slots, write_slots,
+             cu_seqlens, out, scale, eps, status, stream):
     dev = q.device
     if dev.type != "cuda":
-        raise ValueError("gdn_prefill runs on CUDA tensors only")
+        raise ValueError(f"{entry} runs on CUDA tensors only")
     bf = torch.bfloat16
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (a, "a"), (b, "b"), (dt_bias, "dt_bias"), (out, "out")):
         _check(t, n, bf, dev)
@@ -280,12 +298,12 @@ def gdn_prefill(q, k, v, a, b, z, A_log, dt_bias, norm_w, state_pool, read_slots
         raise ValueError("state_pool must be a contiguous fp32 / bf16 / fp16 tensor on the same device")
     if q.dim() != 3 or k.shape != q.shape or v.dim() != 3 or out.shape != v.shape:
         raise ValueError("expected q, k [N, H_k, K] and v, out [N, H_v, V]")
-    # the decode-only size fields are not used by the prefill entry point
+    # the decode-only size fields are not used by the prefill entry points
     dims = make_dims(q, v, state_pool, read_slots.view(-1, 1), k=k, a=a, b=b, z=z, out=out, max_T=1)
     if stream is None:
         stream = torch.cuda.current_stream(dev)
     handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else stream
-    rc = load_library().gdn_prefill(
+    rc = getattr(load_library(), entry)(
         _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(b), _ptr(z), _ptr(A_log), _ptr(dt_bias), _ptr(norm_w),
         _ptr(state_pool), _ptr(read_slots), _ptr(write_slots), _ptr(cu_seqlens), _ptr(out),
         ctypes.byref(dims), float(scale), float(eps), _STATE_DTYPES[state_pool.dtype], _ptr(status), handle)

@@ -1,0 +1,46 @@
+// Internal to libgdnspec: the kernel parameter block shared by the decode /
+// recurrent-prefill translation unit (gdnspec.cu, which also holds every C
+// entry point and its argument checks) and the tensor-core chunked prefill
+// (gdnprefill_chunked.cu).  Not installed; the public interface is
+// include/gdnspec.h.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "gdnspec.h"
+
+namespace gdn_internal {
+
+// Filled on the host from one validated call; passed by value to the kernels.
+struct Params {
+    const __nv_bfloat16* q;
+    const __nv_bfloat16* k;
+    const __nv_bfloat16* v;
+    const __nv_bfloat16* a;
+    const __nv_bfloat16* b;
+    const __nv_bfloat16* z;
+    const float* A_log;
+    const __nv_bfloat16* dt_bias;
+    const __nv_bfloat16* norm_w;
+    void* pool;
+    const int32_t* idx;
+    const int32_t* num_acc;
+    const int32_t* cu;
+    const int32_t* sti;
+    const int32_t* read_slots;   // prefill: start slot per sequence (-1: zero state)
+    const int32_t* write_slots;  // prefill: final-state slot per sequence (-1: none)
+    __nv_bfloat16* out;
+    int32_t* status;
+    int64_t q_stride, k_stride, v_stride, a_stride, b_stride, z_stride, out_stride;
+    int64_t num_slots;
+    int32_t batch, num_tokens, H_k, H_v, stride, max_T, group;
+    float scale, eps;
+};
+
+// Launch the chunked prefill kernel: one CTA per (sequence, v-head) unit.
+cudaError_t launch_prefill_chunked(const Params& p, int64_t units, gdn_dtype state_dtype, cudaStream_t stream);
+
+}  // namespace gdn_internal

@@ -1,0 +1,678 @@
+// libgdnspec: chunked prefill of the Gated DeltaNet layer on the sm_103a
+// tensor cores (tcgen05).  The C entry point gdn_prefill_chunked (gdnspec.cu,
+// declared in include/gdnspec.h) computes what gdn_prefill computes, in the
+// chunked form whose bulk is dense products.
+//
+// Chunked form (C = 64 tokens; S the K x V state at the chunk start; G_t the
+// running sum of the log-decays g inside the chunk; k^, q^ normalised rows):
+//   X = K^ S,  Y = Q^ S                                        (C x V)
+//   A_ts = beta_t e^(G_t - G_s) (k^_t . k^_s)   for s < t       (C x C)
+//   B_t  = beta_t (v_t - e^(G_t) X_t)
+//   (I + A) V' = B                                  (forward substitution)
+//   O_t  = e^(G_t) Y_t + sum_{s<=t} e^(G_t - G_s) (q^_t . k^_s) V'_s
+//   S   <- e^(G_last) S + K~^T V',   K~_s = e^(G_last - G_s) k^_s
+// This is the token recurrence S_t = e^(g_t) S_{t-1} + k^_t v'_t^T with
+// v'_t = beta_t (v_t - (e^(g_t) S_{t-1})^T k^_t) and o_t = S_t^T q^_t, unrolled
+// over the chunk: the same quantities in exact arithmetic.  All decay factors
+// are e^(non-positive), so nothing overflows however strong the decay.
+//
+// Kernel (one CTA of 8 warps per (sequence, v-head), one CTA per SM):
+//  * Products are 128-row tcgen05.mma (kind::f16: bf16 operands, FP32
+//    accumulators) issued by one thread.  Operands are 128-byte-swizzled
+//    K-major tiles in shared memory; accumulators live in tensor memory:
+//      columns   0- 63 P = K^ K^^T         columns  64-127 R = Q^ K^^T
+//      columns 128-255 X = K^ S            columns 256-383 Y = Q^ S
+//      columns 384-511 S (FP32, carried over the whole prompt)
+//      columns   0-127 Z = R~ V' (written once P and R have been read)
+//    Token-row operands hold the chunk in rows 0-63; rows 64-127 are zero
+//    and their results unused.
+//  * The FP32 state stays in tensor memory from the first chunk to the last.
+//    Per chunk it is rescaled by e^(G_last) (tcgen05.ld / st) and K~^T V' is
+//    accumulated into it by one MMA.  Its bf16 image S^T is the B operand of
+//    X and Y for the next chunk.
+//  * The unit lower-triangular solve runs on CUDA cores: one thread per value
+//    column, the column in registers, right-looking so that each step is a
+//    batch of independent FMAs; meanwhile four other warps rescale the state.
+//  * tcgen05.ld / st reach only the 32 TMEM lanes of the warp's quadrant
+//    (warp % 4), which fixes which warps touch which token rows.
+//  * Every wait on the tensor cores is bounded.  On a timeout the CTA sets
+//    GDN_FLAG_TIMEOUT, waits (bounded) for the MMAs in flight, releases its
+//    tensor memory and stops.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "gdn_internal.h"
+#include "gdnspec.h"
+
+namespace {
+
+using gdn_internal::Params;
+
+constexpr int kK = 128;
+constexpr int kV = 128;
+constexpr int kC = 64;                          // tokens per chunk
+constexpr int kThreads = 256;
+constexpr float kQkEps = 1e-6f;                 // inside the L2-norm square root
+constexpr float kSoftplusThreshold = 20.0f;     // softplus(x) = x above this
+constexpr uint32_t kSpinLimit = 1u << 24;       // try_wait polls before giving up (well over 1 s)
+
+// ---- shared memory (offsets from a 1024-byte aligned base) ----------------------
+// 128-byte-swizzled K-major bf16 tiles (the canonical SWIZZLE_128B layout):
+// a tile of R rows is stored in atom columns of 64 elements; element (r, c)
+// sits at (c / 64) * R * 128 + r * 128 + (((c % 64) / 8) ^ (r % 8)) * 16 + (c % 8) * 2.
+constexpr int kTileK = 0;                       // K^    [128 t ][128 kd]
+constexpr int kTileQ = kTileK + 32768;          // Q^    [128 t ][128 kd]
+constexpr int kTileS = kTileQ + 32768;          // S^T   [128 v ][128 kd]
+constexpr int kTileR = kTileS + 32768;          // R~    [128 t ][ 64 s ]
+constexpr int kTileV = kTileR + 16384;          // V'^T  [128 v ][ 64 t ]
+constexpr int kTileKd = kTileV + 16384;         // K~^T  [128 kd][ 64 t ]
+constexpr int kAT = kTileKd + 16384;            // A^T   fp32 [64 s][64 t]
+constexpr int kBStride = kC + 1;                // padded rows: column walks are conflict-free
+constexpr int kBT = kAT + kC * kC * 4;          // B^T   fp32 [128 v][65]
+constexpr int kZStride = kV / 4 + 1;            // uint2 per padded z row
+constexpr int kZ = kBT + kV * kBStride * 4;     // z     bf16 quads [64 t][33]
+constexpr int kMisc = kZ + kC * kZStride * 8;
+
+struct Misc {
+    unsigned long long bar;                     // MMA completion barrier
+    uint32_t tmem;                              // tensor-memory base column
+    int pad;
+    float gamma;                                // e^(G_last) of the current chunk
+    float g[kC], G[kC], beta[kC], eG[kC], kfac[kC];
+    int row[kC];
+    uint2 w[kV / 4];                            // norm weight, bf16 quads
+};
+constexpr int kSmemBytes = kMisc + static_cast<int>(sizeof(Misc)) + 1024;   // + base alignment slack
+static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+
+__device__ __forceinline__ uint32_t swz(int r, int c, int R) {
+    return static_cast<uint32_t>((c >> 6) * R * 128 + r * 128 + ((((c & 63) >> 3) ^ (r & 7)) << 4) + (c & 7) * 2);
+}
+// the 16-byte chunk holding elements 8j .. 8j+7 of row r
+__device__ __forceinline__ uint32_t swz_chunk(int r, int j, int R) {
+    return static_cast<uint32_t>((j >> 3) * R * 128 + r * 128 + (((j & 7) ^ (r & 7)) << 4));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+__device__ __forceinline__ uint4 pack8(const float* x) {
+    return make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]), pack_bf16x2(x[4], x[5]),
+                      pack_bf16x2(x[6], x[7]));
+}
+
+// ---- tcgen05 / mbarrier ---------------------------------------------------------------
+__device__ __forceinline__ uint32_t saddr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// shared-memory matrix descriptor: SWIZZLE_128B, K-major, 8-row groups 1024 B apart
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t addr) {
+    return static_cast<uint64_t>((addr & 0x3FFFF) >> 4) | (static_cast<uint64_t>(16 >> 4) << 16) |
+           (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) |
+           (static_cast<uint64_t>(2) << 61);
+}
+
+// kind::f16 instruction descriptor: FP32 D, bf16 A and B, both K-major
+__device__ __forceinline__ uint32_t idesc_bf16(int M, int N) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
+           (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+
+// D[128][N] (+)= A[128][K] B[N][K]^T over K = 16-element steps; A and B are
+// swizzled K-major tiles of a_rows / b_rows rows
+__device__ __forceinline__ void gemm(uint32_t d, uint32_t a_tile, int a_rows, uint32_t b_tile, int b_rows, int N,
+                                     int K, bool accumulate) {
+    const uint32_t idesc = idesc_bf16(128, N);
+    for (int ks = 0; ks < K / 16; ++ks) {
+        const uint32_t oa = (ks >> 2) * a_rows * 128 + (ks & 3) * 32;
+        const uint32_t ob = (ks >> 2) * b_rows * 128 + (ks & 3) * 32;
+        mma_bf16(d, desc_sw128(a_tile + oa), desc_sw128(b_tile + ob), idesc, (accumulate || ks > 0) ? 1u : 0u);
+    }
+}
+
+__device__ __forceinline__ void commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool wait_parity(uint32_t bar, uint32_t parity) {
+    for (uint32_t it = 0; it < kSpinLimit; ++it) {
+        uint32_t done;
+        asm volatile(
+            "{\n\t.reg .pred P;\n\tmbarrier.try_wait.parity.shared::cta.b64 P, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, P;\n\t}"
+            : "=r"(done)
+            : "r"(bar), "r"(parity)
+            : "memory");
+        if (done) return true;
+    }
+    return false;
+}
+
+__device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+// generic-proxy shared-memory writes become visible to the tensor cores
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// all threads: shared-memory operands written, tensor-memory accesses done
+__device__ __forceinline__ void sync_for_mma() {
+    fence_async_smem();
+    fence_before();
+    __syncthreads();
+    fence_after();
+}
+
+// 32 consecutive FP32 columns of this thread's TMEM lane
+__device__ __forceinline__ void tm_ld32(uint32_t taddr, float (&x)[32]) {
+    uint32_t r[32];
+    __syncwarp();
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(r[j]);
+}
+
+__device__ __forceinline__ void tm_st32(uint32_t taddr, const float (&x)[32]) {
+    __syncwarp();
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(__float_as_uint(x[0])), "r"(__float_as_uint(x[1])), "r"(__float_as_uint(x[2])),
+        "r"(__float_as_uint(x[3])), "r"(__float_as_uint(x[4])), "r"(__float_as_uint(x[5])),
+        "r"(__float_as_uint(x[6])), "r"(__float_as_uint(x[7])), "r"(__float_as_uint(x[8])),
+        "r"(__float_as_uint(x[9])), "r"(__float_as_uint(x[10])), "r"(__float_as_uint(x[11])),
+        "r"(__float_as_uint(x[12])), "r"(__float_as_uint(x[13])), "r"(__float_as_uint(x[14])),
+        "r"(__float_as_uint(x[15])), "r"(__float_as_uint(x[16])), "r"(__float_as_uint(x[17])),
+        "r"(__float_as_uint(x[18])), "r"(__float_as_uint(x[19])), "r"(__float_as_uint(x[20])),
+        "r"(__float_as_uint(x[21])), "r"(__float_as_uint(x[22])), "r"(__float_as_uint(x[23])),
+        "r"(__float_as_uint(x[24])), "r"(__float_as_uint(x[25])), "r"(__float_as_uint(x[26])),
+        "r"(__float_as_uint(x[27])), "r"(__float_as_uint(x[28])), "r"(__float_as_uint(x[29])),
+        "r"(__float_as_uint(x[30])), "r"(__float_as_uint(x[31]))
+        : "memory");
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// ---- element helpers --------------------------------------------------------------------
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) x += __shfl_xor_sync(0xffffffffu, x, m);
+    return x;
+}
+
+__device__ __forceinline__ void unpack4(uint2 raw, float (&x)[4]) {
+    const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.x));
+    const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.y));
+    x[0] = lo.x;
+    x[1] = lo.y;
+    x[2] = hi.x;
+    x[3] = hi.y;
+}
+
+// 32 consecutive state elements of one row <-> FP32, 16-byte streaming accesses
+// (the slot may be read and written by the same CTA, so no read-only loads);
+// stores round to nearest even
+template <typename T> struct RowIO;
+template <> struct RowIO<float> {
+    static __device__ __forceinline__ void load(const float* src, float (&x)[32]) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const float4 f = __ldcs(reinterpret_cast<const float4*>(src) + j);
+            x[4 * j] = f.x;
+            x[4 * j + 1] = f.y;
+            x[4 * j + 2] = f.z;
+            x[4 * j + 3] = f.w;
+        }
+    }
+    static __device__ __forceinline__ void store(float* dst, const float (&x)[32]) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            __stcs(reinterpret_cast<float4*>(dst) + j, make_float4(x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]));
+    }
+};
+template <typename H2> struct RowIO16 {
+    static __device__ __forceinline__ void load(const void* src, float (&x)[32]) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint4 u = __ldcs(reinterpret_cast<const uint4*>(src) + j);
+            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 f = to_float2(*reinterpret_cast<const H2*>(&w[e]));
+                x[8 * j + 2 * e] = f.x;
+                x[8 * j + 2 * e + 1] = f.y;
+            }
+        }
+    }
+    static __device__ __forceinline__ void store(void* dst, const float (&x)[32]) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const H2 hv = from_float2(x[8 * j + 2 * e], x[8 * j + 2 * e + 1]);
+                w[e] = *reinterpret_cast<const uint32_t*>(&hv);
+            }
+            __stcs(reinterpret_cast<uint4*>(dst) + j, make_uint4(w[0], w[1], w[2], w[3]));
+        }
+    }
+    static __device__ __forceinline__ float2 to_float2(__nv_bfloat162 v) { return __bfloat1622float2(v); }
+    static __device__ __forceinline__ float2 to_float2(__half2 v) { return __half22float2(v); }
+    static __device__ __forceinline__ H2 from_float2(float a, float b);
+};
+template <> __device__ __forceinline__ __nv_bfloat162 RowIO16<__nv_bfloat162>::from_float2(float a, float b) {
+    return __floats2bfloat162_rn(a, b);
+}
+template <> __device__ __forceinline__ __half2 RowIO16<__half2>::from_float2(float a, float b) {
+    return __floats2half2_rn(a, b);
+}
+template <> struct RowIO<__nv_bfloat16> : RowIO16<__nv_bfloat162> {};
+template <> struct RowIO<__half> : RowIO16<__half2> {};
+
+// ---- the kernel -------------------------------------------------------------------------
+template <typename StateT>
+__global__ void __launch_bounds__(kThreads, 1) gdn_prefill_chunked_kernel(const Params p) {
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char* sm = smem_raw + ((1024u - (saddr(smem_raw) & 1023u)) & 1023u);
+    Misc& ms = *reinterpret_cast<Misc*>(sm + kMisc);
+    float* AT = reinterpret_cast<float*>(sm + kAT);
+    float* BT = reinterpret_cast<float*>(sm + kBT);
+    uint2* Zq = reinterpret_cast<uint2*>(sm + kZ);
+    const uint32_t sbase = saddr(sm);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int quad = warp & 3;                                  // TMEM lane quadrant of this warp
+    const uint32_t lanes = static_cast<uint32_t>(quad * 32) << 16;
+    const int unit = static_cast<int>(blockIdx.x);
+    const int i = unit / p.H_v;
+    const int h = unit - i * p.H_v;
+    const int kh = h / p.group;
+    const bool gated = p.z != nullptr;
+
+    const int bos = __ldg(p.cu + i);
+    const int L = __ldg(p.cu + i + 1) - bos;
+    const long long rs = __ldg(p.read_slots + i);
+    const long long wsl = __ldg(p.write_slots + i);
+    if (L <= 0) return;
+    if (bos < 0 || bos + L > p.num_tokens) {
+        if (tid == 0 && p.status) atomicOr(p.status, GDN_FLAG_TOKEN_ROW);
+        return;
+    }
+    if (rs >= p.num_slots || wsl >= p.num_slots) {
+        if (tid == 0 && p.status) atomicOr(p.status, GDN_FLAG_SLOT_RANGE);
+        return;
+    }
+
+    // ---- set-up: all 512 TMEM columns, the MMA barrier, the norm weight ----
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(saddr(&ms.tmem)));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    if (tid == 0) {
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(saddr(&ms.bar)));
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (gated && warp == 1) ms.w[lane] = __ldg(reinterpret_cast<const uint2*>(p.norm_w) + lane);
+    // rows 64-127 of the token-row tiles are zero for the whole prompt
+    for (int e = tid; e < 64 * 16; e += kThreads) {
+        const int r = 64 + (e >> 4), j = e & 15;
+        *reinterpret_cast<uint4*>(sm + kTileK + swz_chunk(r, j, 128)) = make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(sm + kTileQ + swz_chunk(r, j, 128)) = make_uint4(0, 0, 0, 0);
+        if (j < 8) *reinterpret_cast<uint4*>(sm + kTileR + swz_chunk(r, j, 128)) = make_uint4(0, 0, 0, 0);
+    }
+    fence_before();
+    __syncthreads();
+    fence_after();
+    const uint32_t tm = ms.tmem;
+    const uint32_t tP = tm, tR = tm + 64, tX = tm + 128, tY = tm + 256, tS = tm + 384, tZ = tm;
+    const uint32_t bar = saddr(&ms.bar);
+    uint32_t phase = 0;
+    bool ok = true;
+
+    // ---- initial state: S (FP32) into TMEM lane kd, its bf16 image into S^T ----
+    if (warp >= 4) {
+        const int kd = quad * 32 + lane;
+        const StateT* src =
+            rs >= 0 ? static_cast<const StateT*>(p.pool) + ((rs * p.H_v + h) * kK + kd) * static_cast<int64_t>(kV)
+                    : nullptr;
+        for (int v0 = 0; v0 < kV; v0 += 32) {
+            float x[32];
+            if (src != nullptr) {
+                RowIO<StateT>::load(src + v0, x);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) x[j] = 0.f;
+            }
+            tm_st32(tS + lanes + v0, x);
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                *reinterpret_cast<__nv_bfloat16*>(sm + kTileS + swz(v0 + j, kd, 128)) = __float2bfloat16_rn(x[j]);
+        }
+    }
+
+    for (int c0 = 0; c0 < L; c0 += kC) {
+        const int n = min(kC, L - c0);
+
+        // ---- per token (8 per warp): k^, q^ rows (bf16 tiles), v (B^T), z, gates.
+        //      Every global load of the chunk is issued before any is used. ----
+        uint2 qraw[8], kraw[8], vraw[8], zraw[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int t = warp + 8 * j;
+            qraw[j] = kraw[j] = vraw[j] = zraw[j] = make_uint2(0, 0);
+            if (t < n) {
+                const int64_t r = bos + c0 + t;
+                qraw[j] = __ldg(reinterpret_cast<const uint2*>(p.q + r * p.q_stride + kh * kK) + lane);
+                kraw[j] = __ldg(reinterpret_cast<const uint2*>(p.k + r * p.k_stride + kh * kK) + lane);
+                vraw[j] = __ldg(reinterpret_cast<const uint2*>(p.v + r * p.v_stride + h * kV) + lane);
+                if (gated) zraw[j] = __ldg(reinterpret_cast<const uint2*>(p.z + r * p.z_stride + h * kV) + lane);
+            }
+        }
+        float ab = 0.f;                                         // lane j: a of token j, lane 8 + j: its b
+        if (lane < 16 && warp + 8 * (lane & 7) < n) {
+            const int64_t r = bos + c0 + warp + 8 * (lane & 7);
+            ab = __bfloat162float(lane < 8 ? p.a[r * p.a_stride + h] : p.b[r * p.b_stride + h]);
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int t = warp + 8 * j;
+            const float a_in = __shfl_sync(0xffffffffu, ab, j);
+            const float b_in = __shfl_sync(0xffffffffu, ab, 8 + j);
+            uint2 kq_k = make_uint2(0, 0), kq_q = make_uint2(0, 0);
+            if (t < n) {
+                float qv[4], kv[4], vv[4];
+                unpack4(qraw[j], qv);
+                unpack4(kraw[j], kv);
+                unpack4(vraw[j], vv);
+                if (gated) Zq[t * kZStride + lane] = zraw[j];
+                float sq = 0.f, sk = 0.f;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    sq += qv[e] * qv[e];
+                    sk += kv[e] * kv[e];
+                }
+                sq = warp_sum(sq);
+                sk = warp_sum(sk);
+                const float rq = rsqrtf(sq + kQkEps) * p.scale;
+                const float rk = rsqrtf(sk + kQkEps);
+                kq_k = make_uint2(pack_bf16x2(kv[0] * rk, kv[1] * rk), pack_bf16x2(kv[2] * rk, kv[3] * rk));
+                kq_q = make_uint2(pack_bf16x2(qv[0] * rq, qv[1] * rq), pack_bf16x2(qv[2] * rq, qv[3] * rq));
+#pragma unroll
+                for (int e = 0; e < 4; ++e) BT[(lane * 4 + e) * kBStride + t] = vv[e];
+                if (lane == 0) {
+                    const float x = a_in + __bfloat162float(p.dt_bias[h]);
+                    const float sp = x > kSoftplusThreshold ? x : log1pf(expf(x));
+                    ms.g[t] = -expf(__ldg(p.A_log + h)) * sp;
+                    ms.beta[t] = 1.0f / (1.0f + expf(-b_in));
+                    ms.row[t] = bos + c0 + t;
+                }
+            } else if (lane == 0) {
+                ms.g[t] = 0.f;
+                ms.beta[t] = 0.f;
+            }
+            *reinterpret_cast<uint2*>(sm + kTileK + swz(t, lane * 4, 128)) = kq_k;
+            *reinterpret_cast<uint2*>(sm + kTileQ + swz(t, lane * 4, 128)) = kq_q;
+        }
+        __syncthreads();
+        if (warp == 0) {
+            // G = inclusive running sum of g; e^(G_t) and e^(G_last - G_t)
+            const float g0 = ms.g[2 * lane], g1 = ms.g[2 * lane + 1];
+            float s = g0 + g1;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float y = __shfl_up_sync(0xffffffffu, s, o);
+                if (lane >= o) s += y;
+            }
+            ms.G[2 * lane] = s - g1;
+            ms.G[2 * lane + 1] = s;
+            __syncwarp();
+            const float G_last = ms.G[n - 1];
+            if (lane == 0) ms.gamma = expf(G_last);
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int t = lane + 32 * e;
+                ms.eG[t] = expf(ms.G[t]);
+                ms.kfac[t] = t < n ? expf(G_last - ms.G[t]) : 0.f;
+            }
+        }
+        __syncthreads();
+        // K~^T [kd][t] = k^_t[kd] e^(G_last - G_t): one 16-byte chunk (8 tokens) per item
+        for (int e = tid; e < kK * (kC / 8); e += kThreads) {
+            const int kd = e & (kK - 1), j = e >> 7;
+            float x[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int t = 8 * j + u;
+                x[u] = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(sm + kTileK + swz(t, kd, 128))) *
+                       ms.kfac[t];
+            }
+            *reinterpret_cast<uint4*>(sm + kTileKd + swz_chunk(kd, j, 128)) = pack8(x);
+        }
+        sync_for_mma();
+
+        // ---- P = K^ K^^T, R = Q^ K^^T, X = K^ S, Y = Q^ S ----
+        if (tid == 0) {
+            gemm(tP, sbase + kTileK, 128, sbase + kTileK, 128, 64, kK, false);
+            gemm(tR, sbase + kTileQ, 128, sbase + kTileK, 128, 64, kK, false);
+            gemm(tX, sbase + kTileK, 128, sbase + kTileS, 128, 128, kK, false);
+            gemm(tY, sbase + kTileQ, 128, sbase + kTileS, 128, 128, kK, false);
+            commit(bar);
+        }
+        ok = !__syncthreads_or(!wait_parity(bar, phase));
+        phase ^= 1;
+        if (!ok) break;
+        fence_after();
+
+        // ---- A^T and R~ from P, R (warps 0, 1); B from X (warps 4, 5); rows t < 64 ----
+        if (quad < 2) {
+            const int t = quad * 32 + lane;
+            const float Gt = ms.G[t], bt = ms.beta[t];
+            const bool live = t < n;
+            if (warp < 4) {
+#pragma unroll
+                for (int s0 = 0; s0 < kC; s0 += 32) {
+                    float x[32];
+                    tm_ld32(tP + lanes + s0, x);
+#pragma unroll
+                    for (int u = 0; u < 32; ++u) {
+                        const int s = s0 + u;
+                        AT[s * kC + t] = (live && s < t) ? bt * __expf(Gt - ms.G[s]) * x[u] : 0.f;
+                    }
+                    tm_ld32(tR + lanes + s0, x);
+#pragma unroll
+                    for (int u = 0; u < 32; ++u) {
+                        const int s = s0 + u;
+                        x[u] = (live && s <= t) ? __expf(Gt - ms.G[s]) * x[u] : 0.f;
+                    }
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        *reinterpret_cast<uint4*>(sm + kTileR + swz_chunk(t, (s0 >> 3) + j, 128)) = pack8(x + 8 * j);
+                }
+            } else {
+                const float eG = ms.eG[t];
+                for (int v0 = 0; v0 < kV; v0 += 32) {
+                    float x[32];
+                    tm_ld32(tX + lanes + v0, x);
+#pragma unroll
+                    for (int u = 0; u < 32; ++u) {
+                        float* bp = &BT[(v0 + u) * kBStride + t];
+                        *bp = live ? bt * (*bp - eG * x[u]) : 0.f;
+                    }
+                }
+            }
+        }
+        fence_before();
+        __syncthreads();
+        fence_after();
+
+        // ---- (I + A) V' = B on warps 0-3 (one value column each);
+        //      S <- e^(G_last) S on warps 4-7 ----
+        if (warp < 4) {
+            const int vc = tid;
+            float x[kC];
+#pragma unroll
+            for (int t = 0; t < kC; ++t) x[t] = BT[vc * kBStride + t];
+            // right-looking: once x[s] is final, remove its part from every later row.
+            // A^T[s][t] is zero for t <= s, so a float4 group may start below s + 1.
+#pragma unroll
+            for (int s = 0; s < kC - 1; ++s) {
+                const float xs = x[s];
+#pragma unroll
+                for (int t4 = (s + 1) >> 2; t4 < kC / 4; ++t4) {
+                    const float4 a4 = *reinterpret_cast<const float4*>(&AT[s * kC + 4 * t4]);
+                    x[4 * t4 + 0] = fmaf(-a4.x, xs, x[4 * t4 + 0]);
+                    x[4 * t4 + 1] = fmaf(-a4.y, xs, x[4 * t4 + 1]);
+                    x[4 * t4 + 2] = fmaf(-a4.z, xs, x[4 * t4 + 2]);
+                    x[4 * t4 + 3] = fmaf(-a4.w, xs, x[4 * t4 + 3]);
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < kC / 8; ++j)
+                *reinterpret_cast<uint4*>(sm + kTileV + swz_chunk(vc, j, 128)) = pack8(x + 8 * j);
+        } else {
+            const float gamma = ms.gamma;
+            for (int v0 = 0; v0 < kV; v0 += 32) {
+                float x[32];
+                tm_ld32(tS + lanes + v0, x);
+#pragma unroll
+                for (int u = 0; u < 32; ++u) x[u] *= gamma;
+                tm_st32(tS + lanes + v0, x);
+            }
+        }
+        sync_for_mma();
+
+        // ---- Z = R~ V',  S += K~^T V' ----
+        if (tid == 0) {
+            gemm(tZ, sbase + kTileR, 128, sbase + kTileV, 128, 128, kC, false);
+            gemm(tS, sbase + kTileKd, 128, sbase + kTileV, 128, 128, kC, true);
+            commit(bar);
+        }
+        ok = !__syncthreads_or(!wait_parity(bar, phase));
+        phase ^= 1;
+        if (!ok) break;
+        fence_after();
+
+        // ---- outputs (warps 0, 1: rows t < 64); next S^T image (warps 4-7) ----
+        if (warp < 2) {
+            const int t = warp * 32 + lane;
+            const float eG = ms.eG[t];
+            float rinv = 1.0f;
+            if (gated) {
+                float ss = 0.f;
+                for (int v0 = 0; v0 < kV; v0 += 32) {
+                    float y[32], z[32];
+                    tm_ld32(tY + lanes + v0, y);
+                    tm_ld32(tZ + lanes + v0, z);
+#pragma unroll
+                    for (int u = 0; u < 32; ++u) {
+                        const float o = fmaf(eG, y[u], z[u]);
+                        ss = fmaf(o, o, ss);
+                    }
+                }
+                rinv = rsqrtf(ss * (1.0f / kV) + p.eps);
+            }
+            const bool live = t < n;
+            __nv_bfloat16* orow = live ? p.out + ms.row[t] * p.out_stride + h * kV : nullptr;
+            for (int v0 = 0; v0 < kV; v0 += 32) {
+                float y[32], z[32];
+                tm_ld32(tY + lanes + v0, y);
+                tm_ld32(tZ + lanes + v0, z);
+                if (!live) continue;
+#pragma unroll
+                for (int j4 = 0; j4 < 8; ++j4) {
+                    float o[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) o[e] = fmaf(eG, y[4 * j4 + e], z[4 * j4 + e]);
+                    if (gated) {
+                        float zz[4], ww[4];
+                        unpack4(Zq[t * kZStride + (v0 >> 2) + j4], zz);
+                        unpack4(ms.w[(v0 >> 2) + j4], ww);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) o[e] = o[e] * rinv * ww[e] * (zz[e] / (1.0f + expf(-zz[e])));
+                    }
+                    *reinterpret_cast<uint2*>(orow + v0 + 4 * j4) =
+                        make_uint2(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]));
+                }
+            }
+        } else if (warp >= 4 && c0 + kC < L) {
+            const int kd = quad * 32 + lane;
+            for (int v0 = 0; v0 < kV; v0 += 32) {
+                float x[32];
+                tm_ld32(tS + lanes + v0, x);
+#pragma unroll
+                for (int u = 0; u < 32; ++u)
+                    *reinterpret_cast<__nv_bfloat16*>(sm + kTileS + swz(v0 + u, kd, 128)) = __float2bfloat16_rn(x[u]);
+            }
+        }
+        fence_before();
+        __syncthreads();
+        fence_after();
+    }
+
+    // ---- the final state to its slot (rounded once), then release TMEM ----
+    if (ok && wsl >= 0 && warp >= 4) {
+        const int kd = quad * 32 + lane;
+        StateT* dst = static_cast<StateT*>(p.pool) + ((wsl * p.H_v + h) * kK + kd) * static_cast<int64_t>(kV);
+        for (int v0 = 0; v0 < kV; v0 += 32) {
+            float x[32];
+            tm_ld32(tS + lanes + v0, x);
+            RowIO<StateT>::store(dst + v0, x);
+        }
+    }
+    if (!ok) {
+        if (tid == 0 && p.status) atomicOr(p.status, GDN_FLAG_TIMEOUT);
+        wait_parity(bar, phase ^ 1u);                           // the MMAs still in flight, bounded
+    }
+    fence_before();
+    __syncthreads();
+    fence_after();
+    if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tm));
+}
+
+template <typename StateT>
+cudaError_t launch(const Params& p, int64_t units, cudaStream_t stream) {
+    static bool done[64] = {false};                             // smem opt-in, once per device
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64 || !done[dev]) {
+        e = cudaFuncSetAttribute(gdn_prefill_chunked_kernel<StateT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kSmemBytes);
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < 64) done[dev] = true;
+    }
+    gdn_prefill_chunked_kernel<StateT><<<static_cast<unsigned>(units), kThreads, kSmemBytes, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+namespace gdn_internal {
+
+cudaError_t launch_prefill_chunked(const Params& p, int64_t units, gdn_dtype state_dtype, cudaStream_t stream) {
+    switch (state_dtype) {
+    case GDN_F32: return launch<float>(p, units, stream);
+    case GDN_BF16: return launch<__nv_bfloat16>(p, units, stream);
+    default: return launch<__half>(p, units, stream);
+    }
+}
+
+}  // namespace gdn_internal

@@ -40,6 +40,7 @@
 
 #include <cstdint>
 
+#include "gdn_internal.h"
 #include "gdnspec.h"
 
 namespace cg = cooperative_groups;
@@ -61,30 +62,7 @@ constexpr int64_t kTile = static_cast<int64_t>(kK) * kV;
 constexpr int kKPad = kK + kK / 4;
 __host__ __device__ constexpr int kpos(int row) { return row + (row >> 4) * 4; }
 
-struct Params {
-    const __nv_bfloat16* q;
-    const __nv_bfloat16* k;
-    const __nv_bfloat16* v;
-    const __nv_bfloat16* a;
-    const __nv_bfloat16* b;
-    const __nv_bfloat16* z;
-    const float* A_log;
-    const __nv_bfloat16* dt_bias;
-    const __nv_bfloat16* norm_w;
-    void* pool;
-    const int32_t* idx;
-    const int32_t* num_acc;
-    const int32_t* cu;
-    const int32_t* sti;
-    const int32_t* read_slots;   // prefill: start slot per sequence (-1: zero state)
-    const int32_t* write_slots;  // prefill: final-state slot per sequence (-1: none)
-    __nv_bfloat16* out;
-    int32_t* status;
-    int64_t q_stride, k_stride, v_stride, a_stride, b_stride, z_stride, out_stride;
-    int64_t num_slots;
-    int32_t batch, num_tokens, H_k, H_v, stride, max_T, group;
-    float scale, eps;
-};
+using gdn_internal::Params;
 
 // per-CTA shared memory
 struct alignas(16) Smem {
@@ -764,6 +742,29 @@ gdn_status gdn_prefill(const void* q, const void* k, const void* v, const void* 
     const int64_t units = static_cast<int64_t>(dims->batch) * dims->H_v;
     const cudaError_t err =
         by_state_dtype<PrefillLauncher>(state_dtype, p, units, reinterpret_cast<cudaStream_t>(stream));
+    return err == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+gdn_status gdn_prefill_chunked(const void* q, const void* k, const void* v, const void* a, const void* b,
+                               const void* z, const float* A_log, const void* dt_bias, const void* norm_w,
+                               void* state_pool, const int32_t* read_slots, const int32_t* write_slots,
+                               const int32_t* cu_seqlens, void* out, const gdn_dims* dims, float scale, float eps,
+                               gdn_dtype state_dtype, int32_t* status_word, gdn_stream_t stream) {
+    const gdn_status ds = check_common_dims(dims);
+    if (ds != GDN_OK) return ds;
+    if (state_dtype != GDN_F32 && state_dtype != GDN_BF16 && state_dtype != GDN_F16) return GDN_ERR_UNSUPPORTED;
+    if (dims->batch == 0) return GDN_OK;
+    if (!read_slots || !write_slots) return GDN_ERR_NULL_ARG;
+    Params p;
+    const gdn_status ps = make_params(p, q, k, v, a, b, z, A_log, dt_bias, norm_w, state_pool, cu_seqlens, out,
+                                      dims, scale, eps, status_word);
+    if (ps != GDN_OK) return ps;
+    if (!aligned(read_slots, 4) || !aligned(write_slots, 4)) return GDN_ERR_MISALIGNED;
+    p.read_slots = read_slots;
+    p.write_slots = write_slots;
+    const int64_t units = static_cast<int64_t>(dims->batch) * dims->H_v;
+    const cudaError_t err =
+        gdn_internal::launch_prefill_chunked(p, units, state_dtype, reinterpret_cast<cudaStream_t>(stream));
     return err == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 

@@ -178,6 +178,7 @@ def make_case(
     pad_prob: float = 0.0,
     extra_rows: int = 0,
     gated: bool = True,
+    A_log_range=(1.0, 16.0),
     seed: int = 0,
 ) -> Case:
     """General seeded case.
@@ -189,6 +190,9 @@ def make_case(
     pad_prob: probability that each slot entry is -1 (CUDA-graph padding).
     extra_rows: non-spec token rows interleaved with the spec rows; when > 0
         the spec rows are gathered through spec_token_indx.
+    A_log_range: A_log = log U(lo, hi); the default gives per-token decays
+        of about e^-0.7 .. e^-11, a small range such as (1e-3, 5e-2) keeps the
+        state alive over hundreds of tokens (long-prompt cases).
     """
     rng = np.random.default_rng(seed)
     stride = T if spec_stride is None else spec_stride
@@ -211,7 +215,7 @@ def make_case(
     z = _bf16(rng, (num_tokens, H_v, V))
     a = _bf16(rng, (num_tokens, H_v))
     b = _bf16(rng, (num_tokens, H_v))
-    A_log = np.log(rng.uniform(1.0, 16.0, H_v)).astype(np.float32)
+    A_log = np.log(rng.uniform(A_log_range[0], A_log_range[1], H_v)).astype(np.float32)
     dt_bias = _bf16(rng, (H_v,))
     norm_w = _bf16(rng, (V,), 1.0, 0.1)
 

@@ -79,6 +79,8 @@ typedef enum { GDN_F32 = 0, GDN_BF16 = 1, GDN_F16 = 2 } gdn_dtype;
 #define GDN_FLAG_QLEN       4  /* q_len > max_T or q_len > spec_stride: sequence skipped */
 #define GDN_FLAG_TOKEN_ROW  8  /* a token row outside [0, num_tokens), or cu_seqlens[i] < 0 or
                                   cu_seqlens[i+1] > cu_seqlens[batch]: sequence skipped */
+#define GDN_FLAG_TIMEOUT    16 /* gdn_prefill_chunked only: a wait on the tensor cores ran past its
+                                  bound; that sequence's outputs and final state are incomplete */
 
 /* Opaque CUDA stream handle; the same type as cudaStream_t (NULL = legacy default stream). */
 typedef struct CUstream_st* gdn_stream_t;
@@ -179,6 +181,41 @@ GDNSPEC_API gdn_status gdn_spec_decode(
  * set GDN_FLAG_TOKEN_ROW.  Asynchronous on `stream`, allocates nothing.
  */
 GDNSPEC_API gdn_status gdn_prefill(
+    const void* q, const void* k, const void* v,
+    const void* a, const void* b, const void* z,
+    const float* A_log, const void* dt_bias, const void* norm_w,
+    void* state_pool,
+    const int32_t* read_slots, const int32_t* write_slots,
+    const int32_t* cu_seqlens,
+    void* out,
+    const gdn_dims* dims, float scale, float eps, gdn_dtype state_dtype,
+    int32_t* status_word, gdn_stream_t stream);
+
+/*
+ * gdn_prefill_chunked -- what gdn_prefill computes, in the chunked form that
+ * runs on the tensor cores: the prompt is cut into chunks of 64 tokens and the
+ * per-token recurrence inside a chunk is unrolled into dense products
+ * ("PR #52191 report", implementation steps 3-4: the inter-chunk recurrence
+ * kernel with all products and the exp(g_last) rescale in FP32 buffers).
+ * With G_t the running sum of the log-decays g inside the chunk, S the state
+ * at its start and k^, q^ the normalised rows:
+ *     (I + A) V' = B,  A_ts = beta_t e^(G_t - G_s) k^_t.k^_s (s < t),
+ *                      B_t  = beta_t (v_t - e^(G_t) S^T k^_t)
+ *     o_t = e^(G_t) S^T q^_t + sum_{s <= t} e^(G_t - G_s) (q^_t.k^_s) v'_s
+ *     S  <- e^(G_last) S + sum_s e^(G_last - G_s) k^_s v'_s^T
+ * which is the same quantity as the token recurrence, in exact arithmetic.
+ * The products take bf16 operands with FP32 accumulation (k^, q^, the bf16
+ * image of S, the decay-weighted scores and V'); the carried state, the
+ * triangular solve and the epilogue are FP32.  The state is rounded to the
+ * pool dtype once, when it is stored at the end of the prompt.
+ *
+ * Arguments, layouts, the caller contract and the status bits are those of
+ * gdn_prefill; in addition GDN_FLAG_TIMEOUT reports a tensor-core wait that
+ * ran past its bound.  One CTA per (sequence, v-head) holding the whole
+ * 512-column tensor memory of its SM; ~212 KB of shared memory.
+ * Asynchronous on `stream`, allocates nothing.
+ */
+GDNSPEC_API gdn_status gdn_prefill_chunked(
     const void* q, const void* k, const void* v,
     const void* a, const void* b, const void* z,
     const float* A_log, const void* dt_bias, const void* norm_w,

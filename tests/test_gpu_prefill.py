@@ -1,7 +1,20 @@
-"""Parity of the prefill entry point (gdn_prefill, through the C-ABI) with the
-oracle's prefill routine: the same per-token step over whole prompts, the
-state carried from a slot (or the zero state) and stored once at the end
-(PR #52191 report, implementation steps 3-4)."""
+"""Parity of the two prefill entry points (gdn_prefill, the per-token
+recurrence, and gdn_prefill_chunked, the tensor-core chunked form; both
+through the C-ABI) with the oracle's prefill routine: the same per-token step
+over whole prompts, the state carried from a slot (or the zero state) and
+stored once at the end (PR #52191 report, implementation steps 3-4).
+
+Tolerances.  The recurrent path computes in FP32 like the decode step and is
+held to the decode step's bounds (PR #51674 report, step 5: output rel L2
+< 5e-4; FP32 state the same; narrow states atol = rtol = 3e-2).  The chunked
+path feeds the tensor cores bf16 operands (k^, q^, the bf16 image of the
+state, the decay-weighted scores and the solved V'), each carrying a relative
+rounding error of at most 2^-9 ~ 2e-3; a product of two such operands and a
+sum over independent terms gives about 2e-3 relative in L2, and the solve and
+the two-term readout keep it of that order.  Its bound is 1e-2 in rel L2
+(the PR #52191 report's kernel checks use atol 1e-2), five times that
+estimate; narrow states keep atol = rtol = 3e-2.
+"""
 from __future__ import annotations
 
 import os
@@ -13,7 +26,7 @@ import torch
 import gated_deltanet_linear_sm_gb300 as gdn
 from gated_deltanet_linear_sm_gb300 import synth
 from oracle import oracle as orc
-from tests.gpu_util import OUT_SENTINEL, TORCH_STATE, device_tensors, make_pool, to_host_bits
+from tests.gpu_util import OUT_SENTINEL, device_tensors, make_pool, to_host_bits
 from tests.util import bf16_values, rel_l2, state_values
 
 pytestmark = pytest.mark.gpu
@@ -21,11 +34,15 @@ pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda", 0)
 THREADS = os.cpu_count() or 1
 
+# entry point -> rel L2 bound for outputs and FP32 states
+ENTRIES = {"recurrent": (gdn.gdn_prefill, 5e-4), "chunked": (gdn.gdn_prefill_chunked, 1e-2)}
+WEAK_DECAY = (1e-3, 5e-2)
 
-def _case(lens, sd, H_k=2, H_v=16, seed=50, gated=True):
+
+def _case(lens, sd, H_k=2, H_v=16, seed=50, gated=True, A_log_range=(1.0, 16.0)):
     return synth.make_case(batch=len(lens), H_k=H_k, H_v=H_v, T=max(lens), state_dtype=sd,
                            num_slots=max(4 * len(lens) + 8, 32), spec_stride=1, q_lens=list(lens),
-                           acc=[1] * len(lens), gated=gated, seed=seed)
+                           acc=[1] * len(lens), gated=gated, A_log_range=A_log_range, seed=seed)
 
 
 def _slots(case, seed, zero_every=3, skip_every=4, in_place=False):
@@ -40,7 +57,8 @@ def _slots(case, seed, zero_every=3, skip_every=4, in_place=False):
     return reads, writes
 
 
-def _run(case, reads, writes):
+def _run(entry, case, reads, writes):
+    fn = ENTRIES[entry][0]
     pool_slots = sorted({int(s) for s in np.concatenate([reads, writes]) if s >= 0})
     pool = make_pool(case, DEV, slots=pool_slots)
     host = to_host_bits(pool)
@@ -48,9 +66,9 @@ def _run(case, reads, writes):
     out = torch.full((case.num_tokens, case.H_v, case.V), OUT_SENTINEL, dtype=torch.int16,
                      device=DEV).view(torch.bfloat16)
     st = torch.zeros(1, dtype=torch.int32, device=DEV)
-    gdn.gdn_prefill(t["q"], t["k"], t["v"], t["a"], t["b"], t["z"], t["A_log"], t["dt_bias"], t["norm_w"],
-                    pool, torch.from_numpy(reads).to(DEV), torch.from_numpy(writes).to(DEV), t["cu_seqlens"],
-                    out, scale=case.scale, eps=case.eps, status=st)
+    fn(t["q"], t["k"], t["v"], t["a"], t["b"], t["z"], t["A_log"], t["dt_bias"], t["norm_w"],
+       pool, torch.from_numpy(reads).to(DEV), torch.from_numpy(writes).to(DEV), t["cu_seqlens"],
+       out, scale=case.scale, eps=case.eps, status=st)
     torch.cuda.synchronize()
     ref = orc.prefill(q=case.q, k=case.k, v=case.v, a=case.a, b=case.b, z=case.z, A_log=case.A_log,
                       dt_bias=case.dt_bias, norm_w=case.norm_w, pool=host, state_dtype=case.state_dtype,
@@ -59,11 +77,14 @@ def _run(case, reads, writes):
     return out, pool, st, ref, host
 
 
-def _check(case, out, pool, st, ref, host, writes):
+def _check(entry, case, out, pool, st, ref, host, writes):
+    tol = ENTRIES[entry][1]
     assert int(st.item()) == 0
     g = bf16_values(out.view(torch.int16).cpu().numpy().view(np.uint16))
     w = bf16_values(ref["out_bf16"])
-    assert rel_l2(g, w) < 5e-4
+    assert np.all(np.isfinite(g))
+    err_out = rel_l2(g, w)
+    assert err_out < tol, err_out
     gp = state_values(to_host_bits(pool), case.state_dtype)
     wp = state_values(host, case.state_dtype)
     wr = [int(s) for s in writes if s >= 0]
@@ -71,41 +92,66 @@ def _check(case, out, pool, st, ref, host, writes):
     # slots nobody writes stay bit-identical
     assert np.array_equal(to_host_bits(pool)[others], host[others])
     if case.state_dtype == synth.F32:
-        assert rel_l2(gp[wr], wp[wr]) < 5e-4
+        err_state = rel_l2(gp[wr], wp[wr])
+        assert err_state < tol, err_state
     else:
         assert np.all(np.abs(gp[wr] - wp[wr]) <= 3e-2 + 3e-2 * np.abs(wp[wr]))
 
 
 @pytest.mark.parametrize("sd", [synth.F32, synth.BF16, synth.F16])
-def test_ragged_prompts(sd):
-    """Prompt lengths across the 8-token rounds (1, 7, 8, 9, 17, 64, 200),
-    zero and slot initial states, some final writes skipped."""
-    case = _case([1, 7, 8, 9, 17, 64, 200], sd)
+@pytest.mark.parametrize("entry", list(ENTRIES))
+def test_ragged_prompts(entry, sd):
+    """Prompt lengths across the 8-token rounds and the 64-token chunks (1, 7,
+    9, 63, 64, 65, 130, 200), zero and slot initial states, some final writes
+    skipped."""
+    case = _case([1, 7, 9, 63, 64, 65, 130, 200], sd)
     reads, writes = _slots(case, 1)
-    _check(case, *_run(case, reads, writes), writes)
+    _check(entry, case, *_run(entry, case, reads, writes), writes)
 
 
-def test_in_place_update():
-    case = _case([5, 33, 12], synth.BF16, seed=51)
+@pytest.mark.parametrize("sd", [synth.F32, synth.BF16])
+@pytest.mark.parametrize("entry", list(ENTRIES))
+def test_long_prompts_weak_decay(entry, sd):
+    """Decays close to 1 keep the state alive across many chunks, so every
+    chunk-to-chunk carry shows in the outputs and the final state."""
+    case = _case([1024, 333], sd, H_k=1, H_v=8, seed=56, A_log_range=WEAK_DECAY)
+    reads, writes = _slots(case, 4, zero_every=2, skip_every=5)
+    _check(entry, case, *_run(entry, case, reads, writes), writes)
+
+
+@pytest.mark.parametrize("entry", list(ENTRIES))
+def test_in_place_update(entry):
+    case = _case([5, 33, 70], synth.BF16, seed=51)
     reads, writes = _slots(case, 2, in_place=True)
-    _check(case, *_run(case, reads, writes), writes)
+    _check(entry, case, *_run(entry, case, reads, writes), writes)
 
 
-def test_ungated_raw_output():
-    case = _case([10, 25], synth.F32, H_k=1, H_v=8, seed=52, gated=False)
+@pytest.mark.parametrize("entry", list(ENTRIES))
+def test_ungated_raw_output(entry):
+    case = _case([10, 90], synth.F32, H_k=1, H_v=8, seed=52, gated=False, A_log_range=WEAK_DECAY)
     reads, writes = _slots(case, 3)
-    _check(case, *_run(case, reads, writes), writes)
+    _check(entry, case, *_run(entry, case, reads, writes), writes)
 
 
-def test_prefill_then_speculative_step():
+@pytest.mark.parametrize("entry", list(ENTRIES))
+def test_extreme_decay_stays_finite(entry):
+    """g of several hundred per token: e^G underflows to zero inside a chunk,
+    and every factor the chunked form uses is e^(non-positive)."""
+    case = _case([3, 100], synth.F32, H_k=1, H_v=8, seed=57, A_log_range=(200.0, 400.0))
+    reads, writes = _slots(case, 5, zero_every=7)
+    _check(entry, case, *_run(entry, case, reads, writes), writes)
+
+
+@pytest.mark.parametrize("entry", list(ENTRIES))
+def test_prefill_then_speculative_step(entry):
     """The state a prefill stores is where the next speculative step rewinds
     to: prefill, then a decode step reading the prefill's slots, against the
     oracle doing the same two calls."""
-    pre = _case([30, 11, 4], synth.F32, H_k=1, H_v=8, seed=53)
+    pre = _case([30, 11, 70], synth.F32, H_k=1, H_v=8, seed=53)
     reads = np.array([-1, -1, -1], np.int32)
     writes = np.array([2, 5, 9], np.int32)
-    out1, pool, st, ref1, host = _run(pre, reads, writes)
-    _check(pre, out1, pool, st, ref1, host, writes)
+    out1, pool, st, ref1, host = _run(entry, pre, reads, writes)
+    _check(entry, pre, out1, pool, st, ref1, host, writes)
     dec = synth.make_case(batch=3, H_k=1, H_v=8, T=3, state_dtype=synth.F32, num_slots=pre.num_slots,
                           acc=[1, 1, 1], seed=54)
     dec.state_indices = np.array([[2, 20, 21], [5, 22, 23], [9, 24, 25]], np.int32)
@@ -115,13 +161,16 @@ def test_prefill_then_speculative_step():
                         pool, t["state_indices"], t["num_accepted"], t["cu_seqlens"], out2, max_T=3)
     torch.cuda.synchronize()
     ref2 = orc.run_case(dec, host)
+    tol = ENTRIES[entry][1]
     g = bf16_values(out2.view(torch.int16).cpu().numpy().view(np.uint16))
-    assert rel_l2(g, bf16_values(ref2["out_bf16"])) < 5e-4
+    assert rel_l2(g, bf16_values(ref2["out_bf16"])) < tol
     w = dec.state_indices[:, :].ravel()
-    assert rel_l2(pool[torch.from_numpy(w.astype(np.int64)).to(DEV)].cpu().numpy(), host[w]) < 5e-4
+    assert rel_l2(pool[torch.from_numpy(w.astype(np.int64)).to(DEV)].cpu().numpy(), host[w]) < tol
 
 
-def test_bad_slot_is_flagged_and_skipped():
+@pytest.mark.parametrize("entry", list(ENTRIES))
+def test_bad_slot_is_flagged_and_skipped(entry):
+    fn = ENTRIES[entry][0]
     case = _case([6, 6, 6], synth.F32, H_k=1, H_v=8, seed=55)
     reads = np.array([1, case.num_slots + 3, 4], np.int32)
     writes = np.array([7, 8, 9], np.int32)
@@ -130,10 +179,23 @@ def test_bad_slot_is_flagged_and_skipped():
     t = device_tensors(case, DEV)
     out = torch.zeros(case.num_tokens, case.H_v, case.V, dtype=torch.bfloat16, device=DEV)
     st = torch.zeros(1, dtype=torch.int32, device=DEV)
-    gdn.gdn_prefill(t["q"], t["k"], t["v"], t["a"], t["b"], t["z"], t["A_log"], t["dt_bias"], t["norm_w"],
-                    pool, torch.from_numpy(reads).to(DEV), torch.from_numpy(writes).to(DEV), t["cu_seqlens"],
-                    out, status=st)
+    fn(t["q"], t["k"], t["v"], t["a"], t["b"], t["z"], t["A_log"], t["dt_bias"], t["norm_w"],
+       pool, torch.from_numpy(reads).to(DEV), torch.from_numpy(writes).to(DEV), t["cu_seqlens"],
+       out, status=st)
     torch.cuda.synchronize()
     assert int(st.item()) & gdn.binding.GDN_FLAG_SLOT_RANGE
     assert torch.equal(pool[8].view(torch.int32), before[8].view(torch.int32))
     assert not torch.equal(pool[7].view(torch.int32), before[7].view(torch.int32))
+
+
+@pytest.mark.parametrize("entry", list(ENTRIES))
+def test_empty_prompts_touch_nothing(entry):
+    """Zero-length prompts between real ones: no output rows of theirs exist,
+    their write slots stay as they were."""
+    fn = ENTRIES[entry][0]
+    case = _case([0, 20, 0, 5], synth.F32, H_k=1, H_v=8, seed=58)
+    reads = np.array([1, 2, 3, 4], np.int32)
+    writes = np.array([10, 11, 12, 13], np.int32)
+    out, pool, st, ref, host = _run(entry, case, reads, writes)
+    assert np.array_equal(to_host_bits(pool)[[10, 12]], host[[10, 12]])
+    _check(entry, case, out, pool, st, ref, host, np.array([-1, 11, -1, 13], np.int32))
