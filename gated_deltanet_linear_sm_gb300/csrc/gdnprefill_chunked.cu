@@ -21,20 +21,18 @@
 //    accumulators) issued by one thread.  Operands are 128-byte-swizzled
 //    K-major tiles in shared memory; accumulators live in tensor memory:
 //      columns   0- 63 P = K^ K^^T         columns  64-127 R = Q^ K^^T
-//      columns 128-255 X = K^ S            columns 256-383 Y = Q^ S
-//      columns 384-511 S (FP32, carried over the whole prompt)
-//      columns   0-127 Z = R~ V' (written once P and R have been read)
+//      columns 128-255 X = K^ S            columns 256-383 O = Q^ S, then
+//                                          e^G O + R~ V' (the chunk's output)
+//      columns 384-511 S^T (FP32, carried over the whole prompt)
 //    Token-row operands hold the chunk in rows 0-63; rows 64-127 are zero
 //    and their results unused.
 //  * The FP32 state stays in tensor memory from the first chunk to the last.
-//    Per chunk it is rescaled by e^(G_last) (tcgen05.ld / st) and K~^T V' is
-//    accumulated into it by one MMA.  Its bf16 image S^T is the B operand of
-//    X and Y for the next chunk.
-//  * The unit lower-triangular solve runs on CUDA cores: one thread per value
-//    column, the column in registers, right-looking so that each step is a
-//    batch of independent FMAs; meanwhile four other warps rescale the state.
-//  * tcgen05.ld / st reach only the 32 TMEM lanes of the warp's quadrant
-//    (warp % 4), which fixes which warps touch which token rows.
+//    Per chunk it is rescaled by e^(G_last) (tcgen05.ld / st) and V'^T K~ is
+//    accumulated into it by one MMA.  Its bf16 image is the B operand of X
+//    and O for the next chunk.
+//  * The unit lower-triangular solve runs on CUDA cores, two threads per
+//    value column with the column in registers, right-looking so that each
+//    step is a batch of independent FMAs.
 //  * Every wait on the tensor cores is bounded.  On a timeout the CTA sets
 //    GDN_FLAG_TIMEOUT, waits (bounded) for the MMAs in flight, releases its
 //    tensor memory and stops.
@@ -42,6 +40,7 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <cstddef>
 #include <cstdint>
 
 #include "gdn_internal.h"
@@ -69,9 +68,12 @@ constexpr int kTileS = kTileQ + 32768;          // S^T   [128 v ][128 kd]
 constexpr int kTileR = kTileS + 32768;          // R~    [128 t ][ 64 s ]
 constexpr int kTileV = kTileR + 16384;          // V'^T  [128 v ][ 64 t ]
 constexpr int kTileKd = kTileV + 16384;         // K~^T  [128 kd][ 64 t ]
-constexpr int kAT = kTileKd + 16384;            // A^T   fp32 [64 s][64 t]
-constexpr int kBStride = kC + 1;                // padded rows: column walks are conflict-free
-constexpr int kBT = kAT + kC * kC * 4;          // B^T   fp32 [128 v][65]
+constexpr int kA2Half = 36;                     // floats per parity half-row (32 used; the pad puts
+                                                // the two halves of a row on different banks)
+constexpr int kA2Row = 2 * kA2Half;
+constexpr int kA2 = kTileKd + 16384;            // A     fp32 [64 s][2 parity][36 (t/2)]
+constexpr int kBStride = kC + 1;                // odd row pitch: column walks are conflict-free
+constexpr int kBT = kA2 + kC * kA2Row * 4;      // B^T   fp32 [128 v][65]
 constexpr int kZStride = kV / 4 + 1;            // uint2 per padded z row
 constexpr int kZ = kBT + kV * kBStride * 4;     // z     bf16 quads [64 t][33]
 constexpr int kMisc = kZ + kC * kZStride * 8;
@@ -79,12 +81,13 @@ constexpr int kMisc = kZ + kC * kZStride * 8;
 struct Misc {
     unsigned long long bar;                     // MMA completion barrier
     uint32_t tmem;                              // tensor-memory base column
-    int pad;
     float gamma;                                // e^(G_last) of the current chunk
-    float g[kC], G[kC], beta[kC], eG[kC], kfac[kC];
+    float g[kC], G[kC], beta[kC], eG[kC], kfac[kC];   // G 16-byte aligned (float4 reads)
+    float ssq[2][kC];                           // per-row sums of squares of the two column halves
     int row[kC];
     uint2 w[kV / 4];                            // norm weight, bf16 quads
 };
+static_assert(kMisc % 16 == 0 && offsetof(Misc, G) % 16 == 0, "float4 reads of G");
 constexpr int kSmemBytes = kMisc + static_cast<int>(sizeof(Misc)) + 1024;   // + base alignment slack
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 
@@ -213,12 +216,6 @@ __device__ __forceinline__ void tm_st32(uint32_t taddr, const float (&x)[32]) {
 }
 
 // ---- element helpers --------------------------------------------------------------------
-__device__ __forceinline__ float warp_sum(float x) {
-#pragma unroll
-    for (int m = 16; m >= 1; m >>= 1) x += __shfl_xor_sync(0xffffffffu, x, m);
-    return x;
-}
-
 __device__ __forceinline__ void unpack4(uint2 raw, float (&x)[4]) {
     const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.x));
     const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.y));
@@ -228,79 +225,66 @@ __device__ __forceinline__ void unpack4(uint2 raw, float (&x)[4]) {
     x[3] = hi.y;
 }
 
-// 32 consecutive state elements of one row <-> FP32, 16-byte streaming accesses
-// (the slot may be read and written by the same CTA, so no read-only loads);
-// stores round to nearest even
-template <typename T> struct RowIO;
-template <> struct RowIO<float> {
-    static __device__ __forceinline__ void load(const float* src, float (&x)[32]) {
+// one state element <-> FP32 (the slot may be read and written by the same
+// CTA, so no read-only loads); stores round to nearest even
+__device__ __forceinline__ float load_elem(const float* p) { return __ldcs(p); }
+__device__ __forceinline__ float load_elem(const __nv_bfloat16* p) { return __bfloat162float(*p); }
+__device__ __forceinline__ float load_elem(const __half* p) { return __half2float(*p); }
+__device__ __forceinline__ void store_elem(float* p, float x) { __stcs(p, x); }
+__device__ __forceinline__ void store_elem(__nv_bfloat16* p, float x) { *p = __float2bfloat16_rn(x); }
+__device__ __forceinline__ void store_elem(__half* p, float x) { *p = __float2half_rn(x); }
+
+// d[u] = e^(Gt - G[u]) for 32 consecutive entries of G (16-byte aligned)
+__device__ __forceinline__ void load_decays(const float* G, float Gt, float (&d)[32]) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const float4 f = __ldcs(reinterpret_cast<const float4*>(src) + j);
-            x[4 * j] = f.x;
-            x[4 * j + 1] = f.y;
-            x[4 * j + 2] = f.z;
-            x[4 * j + 3] = f.w;
-        }
+    for (int j = 0; j < 8; ++j) {
+        const float4 g4 = reinterpret_cast<const float4*>(G)[j];
+        d[4 * j] = __expf(Gt - g4.x);
+        d[4 * j + 1] = __expf(Gt - g4.y);
+        d[4 * j + 2] = __expf(Gt - g4.z);
+        d[4 * j + 3] = __expf(Gt - g4.w);
     }
-    static __device__ __forceinline__ void store(float* dst, const float (&x)[32]) {
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-            __stcs(reinterpret_cast<float4*>(dst) + j, make_float4(x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]));
-    }
-};
-template <typename H2> struct RowIO16 {
-    static __device__ __forceinline__ void load(const void* src, float (&x)[32]) {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const uint4 u = __ldcs(reinterpret_cast<const uint4*>(src) + j);
-            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float2 f = to_float2(*reinterpret_cast<const H2*>(&w[e]));
-                x[8 * j + 2 * e] = f.x;
-                x[8 * j + 2 * e + 1] = f.y;
-            }
-        }
-    }
-    static __device__ __forceinline__ void store(void* dst, const float (&x)[32]) {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            uint32_t w[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const H2 hv = from_float2(x[8 * j + 2 * e], x[8 * j + 2 * e + 1]);
-                w[e] = *reinterpret_cast<const uint32_t*>(&hv);
-            }
-            __stcs(reinterpret_cast<uint4*>(dst) + j, make_uint4(w[0], w[1], w[2], w[3]));
-        }
-    }
-    static __device__ __forceinline__ float2 to_float2(__nv_bfloat162 v) { return __bfloat1622float2(v); }
-    static __device__ __forceinline__ float2 to_float2(__half2 v) { return __half22float2(v); }
-    static __device__ __forceinline__ H2 from_float2(float a, float b);
-};
-template <> __device__ __forceinline__ __nv_bfloat162 RowIO16<__nv_bfloat162>::from_float2(float a, float b) {
-    return __floats2bfloat162_rn(a, b);
 }
-template <> __device__ __forceinline__ __half2 RowIO16<__half2>::from_float2(float a, float b) {
-    return __floats2half2_rn(a, b);
-}
-template <> struct RowIO<__nv_bfloat16> : RowIO16<__nv_bfloat162> {};
-template <> struct RowIO<__half> : RowIO16<__half2> {};
+
+// silu(z) = z sigmoid(z); exp overflow for very negative z gives 1/inf = 0
+__device__ __forceinline__ float silu(float z) { return z * __frcp_rn(1.0f + __expf(-z)); }
 
 // ---- the kernel -------------------------------------------------------------------------
+//
+// Per chunk, with the warps' TMEM quadrants q = warp % 4 (tcgen05.ld / st reach
+// only lanes 32q .. 32q + 31, so token rows 0-63 are reachable from warps 0, 1,
+// 4, 5 only):
+//   phase 1  all warps        k^, q^, v, z, gates of the chunk's 64 tokens; the
+//                             running sum G; K~^T
+//   MMA 1                     P = K^ K^^T, R = Q^ K^^T, X = K^ S, O = Q^ S
+//   phase 2  warps 0,1        A from P; B = beta (v - e^G X) and O <- e^G O for
+//                             v < 64
+//            warps 4,5        R~ from R; the same for v >= 64
+//            all warps        S^T <- e^(G_last) S^T (their quadrant's rows, half
+//                             of the columns each)
+//   phase 3  all warps        (I + A) V' = B: two threads per value column,
+//                             rows split by parity; the V'^T tile
+//   MMA 2                     O += R~ V',  S^T += V'^T K~
+//   phase 4  warps 0,1,4,5    the gated RMSNorm epilogue of the chunk's rows
+//                             (each warp half of the columns); then all warps
+//                             write the bf16 image of S^T for the next chunk
+//
+// The state lives transposed in tensor memory (lane v, column kd), so its
+// bf16 image, the K-major [v][kd] operand, is written row by row.
 template <typename StateT>
 __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_chunked_kernel(const Params p) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char* sm = smem_raw + ((1024u - (saddr(smem_raw) & 1023u)) & 1023u);
     Misc& ms = *reinterpret_cast<Misc*>(sm + kMisc);
-    float* AT = reinterpret_cast<float*>(sm + kAT);
+    float* A2 = reinterpret_cast<float*>(sm + kA2);
     float* BT = reinterpret_cast<float*>(sm + kBT);
     uint2* Zq = reinterpret_cast<uint2*>(sm + kZ);
     const uint32_t sbase = saddr(sm);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quad = warp & 3;                                  // TMEM lane quadrant of this warp
+    const int half = warp >> 2;                                 // which half of the columns
     const uint32_t lanes = static_cast<uint32_t>(quad * 32) << 16;
+    const int row = quad * 32 + lane;                           // this thread's TMEM lane
     const int unit = static_cast<int>(blockIdx.x);
     const int i = unit / p.H_v;
     const int h = unit - i * p.H_v;
@@ -342,47 +326,52 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_chunked_kernel(const 
     __syncthreads();
     fence_after();
     const uint32_t tm = ms.tmem;
-    const uint32_t tP = tm, tR = tm + 64, tX = tm + 128, tY = tm + 256, tS = tm + 384, tZ = tm;
+    const uint32_t tP = tm, tR = tm + 64, tX = tm + 128, tO = tm + 256, tS = tm + 384;
     const uint32_t bar = saddr(&ms.bar);
     uint32_t phase = 0;
     bool ok = true;
 
-    // ---- initial state: S (FP32) into TMEM lane kd, its bf16 image into S^T ----
-    if (warp >= 4) {
-        const int kd = quad * 32 + lane;
+    // ---- initial state: S^T (FP32) into TMEM lane v, its bf16 image into the S^T tile.
+    //      Thread (v, half) covers kd in [64 half, 64 half + 64); a warp reads 32
+    //      consecutive v of one kd row per load. ----
+    {
         const StateT* src =
-            rs >= 0 ? static_cast<const StateT*>(p.pool) + ((rs * p.H_v + h) * kK + kd) * static_cast<int64_t>(kV)
+            rs >= 0 ? static_cast<const StateT*>(p.pool) + (rs * p.H_v + h) * static_cast<int64_t>(kK * kV) + row
                     : nullptr;
-        for (int v0 = 0; v0 < kV; v0 += 32) {
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+            const int kd0 = 64 * half + 32 * c;
             float x[32];
-            if (src != nullptr) {
-                RowIO<StateT>::load(src + v0, x);
-            } else {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) x[j] = 0.f;
-            }
-            tm_st32(tS + lanes + v0, x);
+            for (int j = 0; j < 32; ++j) x[j] = src ? load_elem(src + (kd0 + j) * kV) : 0.f;
+            tm_st32(tS + lanes + kd0, x);
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-                *reinterpret_cast<__nv_bfloat16*>(sm + kTileS + swz(v0 + j, kd, 128)) = __float2bfloat16_rn(x[j]);
+            for (int j = 0; j < 4; ++j)
+                *reinterpret_cast<uint4*>(sm + kTileS + swz_chunk(row, (kd0 >> 3) + j, 128)) = pack8(x + 8 * j);
         }
     }
 
     for (int c0 = 0; c0 < L; c0 += kC) {
         const int n = min(kC, L - c0);
 
-        // ---- per token (8 per warp): k^, q^ rows (bf16 tiles), v (B^T), z, gates.
-        //      Every global load of the chunk is issued before any is used. ----
-        uint2 qraw[8], kraw[8], vraw[8], zraw[8];
+        // ---- phase 1: per token (8 per warp) k^, q^ (bf16 tiles), v (B^T), z, gates.
+        //      Every global load of the chunk is issued before any is used; v is
+        //      read one element per lane per load (v = lane + 32 e) so that its
+        //      transposed store into B^T hits 32 distinct banks. ----
+        uint2 qraw[8], kraw[8], zraw[8];
+        __nv_bfloat16 vraw[8][4];
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             const int t = warp + 8 * j;
-            qraw[j] = kraw[j] = vraw[j] = zraw[j] = make_uint2(0, 0);
+            qraw[j] = kraw[j] = zraw[j] = make_uint2(0, 0);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) vraw[j][e] = __float2bfloat16_rn(0.f);
             if (t < n) {
                 const int64_t r = bos + c0 + t;
                 qraw[j] = __ldg(reinterpret_cast<const uint2*>(p.q + r * p.q_stride + kh * kK) + lane);
                 kraw[j] = __ldg(reinterpret_cast<const uint2*>(p.k + r * p.k_stride + kh * kK) + lane);
-                vraw[j] = __ldg(reinterpret_cast<const uint2*>(p.v + r * p.v_stride + h * kV) + lane);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) vraw[j][e] = p.v[r * p.v_stride + h * kV + lane + 32 * e];
                 if (gated) zraw[j] = __ldg(reinterpret_cast<const uint2*>(p.z + r * p.z_stride + h * kV) + lane);
             }
         }
@@ -391,49 +380,59 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_chunked_kernel(const 
             const int64_t r = bos + c0 + warp + 8 * (lane & 7);
             ab = __bfloat162float(lane < 8 ? p.a[r * p.a_stride + h] : p.b[r * p.b_stride + h]);
         }
+        {
+            // gates of the warp's 8 tokens, one per lane
+            const float b_in = __shfl_down_sync(0xffffffffu, ab, 8);
+            const int t = warp + 8 * lane;
+            if (lane < 8) {
+                float g = 0.f, beta = 0.f;
+                if (t < n) {
+                    const float x = ab + __bfloat162float(p.dt_bias[h]);
+                    const float sp = x > kSoftplusThreshold ? x : log1pf(expf(x));
+                    g = -expf(__ldg(p.A_log + h)) * sp;
+                    beta = 1.0f / (1.0f + expf(-b_in));
+                    ms.row[t] = bos + c0 + t;
+                }
+                ms.g[t] = g;
+                ms.beta[t] = beta;
+            }
+        }
+        // squared norms of the 8 q and 8 k rows, reduced together
+        float sums[16];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            float qv[4], kv[4];
+            unpack4(qraw[j], qv);
+            unpack4(kraw[j], kv);
+            sums[j] = qv[0] * qv[0] + qv[1] * qv[1] + qv[2] * qv[2] + qv[3] * qv[3];
+            sums[8 + j] = kv[0] * kv[0] + kv[1] * kv[1] + kv[2] * kv[2] + kv[3] * kv[3];
+        }
+#pragma unroll
+        for (int m = 16; m >= 1; m >>= 1)
+#pragma unroll
+            for (int j = 0; j < 16; ++j) sums[j] += __shfl_xor_sync(0xffffffffu, sums[j], m);
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             const int t = warp + 8 * j;
-            const float a_in = __shfl_sync(0xffffffffu, ab, j);
-            const float b_in = __shfl_sync(0xffffffffu, ab, 8 + j);
-            uint2 kq_k = make_uint2(0, 0), kq_q = make_uint2(0, 0);
+            uint2 kk = make_uint2(0, 0), qq = make_uint2(0, 0);
             if (t < n) {
-                float qv[4], kv[4], vv[4];
+                float qv[4], kv[4];
                 unpack4(qraw[j], qv);
                 unpack4(kraw[j], kv);
-                unpack4(vraw[j], vv);
                 if (gated) Zq[t * kZStride + lane] = zraw[j];
-                float sq = 0.f, sk = 0.f;
+                const float rq = rsqrtf(sums[j] + kQkEps) * p.scale;
+                const float rk = rsqrtf(sums[8 + j] + kQkEps);
+                kk = make_uint2(pack_bf16x2(kv[0] * rk, kv[1] * rk), pack_bf16x2(kv[2] * rk, kv[3] * rk));
+                qq = make_uint2(pack_bf16x2(qv[0] * rq, qv[1] * rq), pack_bf16x2(qv[2] * rq, qv[3] * rq));
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    sq += qv[e] * qv[e];
-                    sk += kv[e] * kv[e];
-                }
-                sq = warp_sum(sq);
-                sk = warp_sum(sk);
-                const float rq = rsqrtf(sq + kQkEps) * p.scale;
-                const float rk = rsqrtf(sk + kQkEps);
-                kq_k = make_uint2(pack_bf16x2(kv[0] * rk, kv[1] * rk), pack_bf16x2(kv[2] * rk, kv[3] * rk));
-                kq_q = make_uint2(pack_bf16x2(qv[0] * rq, qv[1] * rq), pack_bf16x2(qv[2] * rq, qv[3] * rq));
-#pragma unroll
-                for (int e = 0; e < 4; ++e) BT[(lane * 4 + e) * kBStride + t] = vv[e];
-                if (lane == 0) {
-                    const float x = a_in + __bfloat162float(p.dt_bias[h]);
-                    const float sp = x > kSoftplusThreshold ? x : log1pf(expf(x));
-                    ms.g[t] = -expf(__ldg(p.A_log + h)) * sp;
-                    ms.beta[t] = 1.0f / (1.0f + expf(-b_in));
-                    ms.row[t] = bos + c0 + t;
-                }
-            } else if (lane == 0) {
-                ms.g[t] = 0.f;
-                ms.beta[t] = 0.f;
+                for (int e = 0; e < 4; ++e) BT[(lane + 32 * e) * kBStride + t] = __bfloat162float(vraw[j][e]);
             }
-            *reinterpret_cast<uint2*>(sm + kTileK + swz(t, lane * 4, 128)) = kq_k;
-            *reinterpret_cast<uint2*>(sm + kTileQ + swz(t, lane * 4, 128)) = kq_q;
+            *reinterpret_cast<uint2*>(sm + kTileK + swz(t, lane * 4, 128)) = kk;
+            *reinterpret_cast<uint2*>(sm + kTileQ + swz(t, lane * 4, 128)) = qq;
         }
         __syncthreads();
         if (warp == 0) {
-            // G = inclusive running sum of g; e^(G_t) and e^(G_last - G_t)
+            // G = inclusive running sum of g; e^(G_t), e^(G_last - G_t), e^(G_last)
             const float g0 = ms.g[2 * lane], g1 = ms.g[2 * lane + 1];
             float s = g0 + g1;
 #pragma unroll
@@ -468,12 +467,12 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_chunked_kernel(const 
         }
         sync_for_mma();
 
-        // ---- P = K^ K^^T, R = Q^ K^^T, X = K^ S, Y = Q^ S ----
+        // ---- MMA 1: P = K^ K^^T, R = Q^ K^^T, X = K^ S, O = Q^ S ----
         if (tid == 0) {
             gemm(tP, sbase + kTileK, 128, sbase + kTileK, 128, 64, kK, false);
-            gemm(tR, sbase + kTileQ, 128, sbase + kTileK, 128, 64, kK, false);
             gemm(tX, sbase + kTileK, 128, sbase + kTileS, 128, 128, kK, false);
-            gemm(tY, sbase + kTileQ, 128, sbase + kTileS, 128, 128, kK, false);
+            gemm(tO, sbase + kTileQ, 128, sbase + kTileS, 128, 128, kK, false);
+            gemm(tR, sbase + kTileQ, 128, sbase + kTileK, 128, 64, kK, false);
             commit(bar);
         }
         ok = !__syncthreads_or(!wait_parity(bar, phase));
@@ -481,88 +480,114 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_chunked_kernel(const 
         if (!ok) break;
         fence_after();
 
-        // ---- A^T and R~ from P, R (warps 0, 1); B from X (warps 4, 5); rows t < 64 ----
+        // ---- phase 2 ----
         if (quad < 2) {
-            const int t = quad * 32 + lane;
+            const int t = row;                                  // token row of this lane
             const float Gt = ms.G[t], bt = ms.beta[t];
             const bool live = t < n;
-            if (warp < 4) {
+            if (half == 0) {
+                // A (s < t) from P, stored as A2[s][t % 2][t / 2]; the decay
+                // factors are formed before any store, so no shared load waits
+                // behind a store
+                float* dst = A2 + (t & 1) * kA2Half + (t >> 1);
 #pragma unroll
                 for (int s0 = 0; s0 < kC; s0 += 32) {
-                    float x[32];
+                    float x[32], d[32];
+                    load_decays(ms.G + s0, Gt, d);
                     tm_ld32(tP + lanes + s0, x);
 #pragma unroll
                     for (int u = 0; u < 32; ++u) {
                         const int s = s0 + u;
-                        AT[s * kC + t] = (live && s < t) ? bt * __expf(Gt - ms.G[s]) * x[u] : 0.f;
+                        dst[s * kA2Row] = (live && s < t) ? bt * d[u] * x[u] : 0.f;
                     }
+                }
+            } else {
+                // R~ (s <= t) from R
+#pragma unroll
+                for (int s0 = 0; s0 < kC; s0 += 32) {
+                    float x[32], d[32];
+                    load_decays(ms.G + s0, Gt, d);
                     tm_ld32(tR + lanes + s0, x);
 #pragma unroll
                     for (int u = 0; u < 32; ++u) {
                         const int s = s0 + u;
-                        x[u] = (live && s <= t) ? __expf(Gt - ms.G[s]) * x[u] : 0.f;
+                        x[u] = (live && s <= t) ? d[u] * x[u] : 0.f;
                     }
 #pragma unroll
                     for (int j = 0; j < 4; ++j)
                         *reinterpret_cast<uint4*>(sm + kTileR + swz_chunk(t, (s0 >> 3) + j, 128)) = pack8(x + 8 * j);
                 }
-            } else {
-                const float eG = ms.eG[t];
-                for (int v0 = 0; v0 < kV; v0 += 32) {
-                    float x[32];
-                    tm_ld32(tX + lanes + v0, x);
+            }
+            // B = beta (v - e^(G_t) X) and O <- e^(G_t) O for this half of the value columns
+            const float eG = ms.eG[t];
 #pragma unroll
-                    for (int u = 0; u < 32; ++u) {
-                        float* bp = &BT[(v0 + u) * kBStride + t];
-                        *bp = live ? bt * (*bp - eG * x[u]) : 0.f;
-                    }
+            for (int c = 0; c < 2; ++c) {
+                const int v0 = 64 * half + 32 * c;
+                float x[32];
+                tm_ld32(tX + lanes + v0, x);
+#pragma unroll
+                for (int u = 0; u < 32; ++u) {
+                    float* bp = &BT[(v0 + u) * kBStride + t];
+                    *bp = live ? bt * (*bp - eG * x[u]) : 0.f;
                 }
+                tm_ld32(tO + lanes + v0, x);
+#pragma unroll
+                for (int u = 0; u < 32; ++u) x[u] *= eG;
+                tm_st32(tO + lanes + v0, x);
+            }
+        }
+        {
+            // S^T <- e^(G_last) S^T: lane v of this quadrant, this half of the kd columns
+            const float gamma = ms.gamma;
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                const uint32_t col = tS + lanes + 64 * half + 32 * c;
+                float x[32];
+                tm_ld32(col, x);
+#pragma unroll
+                for (int u = 0; u < 32; ++u) x[u] *= gamma;
+                tm_st32(col, x);
             }
         }
         fence_before();
         __syncthreads();
         fence_after();
 
-        // ---- (I + A) V' = B on warps 0-3 (one value column each);
-        //      S <- e^(G_last) S on warps 4-7 ----
-        if (warp < 4) {
-            const int vc = tid;
-            float x[kC];
+        // ---- phase 3: (I + A) V' = B.  Thread pair (2 vc, 2 vc + 1) of a warp
+        //      solves value column vc; member r owns rows t = 2 i + r in x[i].
+        //      Right-looking: once x_s is final its owner broadcasts it and both
+        //      remove its part from their later rows (A2[s][.][i] is zero for
+        //      rows t <= s, so the float4 groups may start below s + 1). ----
+        {
+            const int vc = warp * 16 + (lane >> 1), r = lane & 1;
+            float x[32];
 #pragma unroll
-            for (int t = 0; t < kC; ++t) x[t] = BT[vc * kBStride + t];
-            // right-looking: once x[s] is final, remove its part from every later row.
-            // A^T[s][t] is zero for t <= s, so a float4 group may start below s + 1.
+            for (int i2 = 0; i2 < 32; ++i2) x[i2] = BT[vc * kBStride + 2 * i2 + r];
+            const float* arow = A2 + r * kA2Half;
 #pragma unroll
             for (int s = 0; s < kC - 1; ++s) {
-                const float xs = x[s];
+                const float mine = (r == (s & 1)) ? x[s >> 1] : 0.f;
+                const float xs = __shfl_sync(0xffffffffu, mine, (lane & ~1) | (s & 1));
 #pragma unroll
-                for (int t4 = (s + 1) >> 2; t4 < kC / 4; ++t4) {
-                    const float4 a4 = *reinterpret_cast<const float4*>(&AT[s * kC + 4 * t4]);
-                    x[4 * t4 + 0] = fmaf(-a4.x, xs, x[4 * t4 + 0]);
-                    x[4 * t4 + 1] = fmaf(-a4.y, xs, x[4 * t4 + 1]);
-                    x[4 * t4 + 2] = fmaf(-a4.z, xs, x[4 * t4 + 2]);
-                    x[4 * t4 + 3] = fmaf(-a4.w, xs, x[4 * t4 + 3]);
+                for (int i4 = (s >> 3); i4 < 8; ++i4) {
+                    const float4 a4 = *reinterpret_cast<const float4*>(arow + s * kA2Row + 4 * i4);
+                    x[4 * i4 + 0] = fmaf(-a4.x, xs, x[4 * i4 + 0]);
+                    x[4 * i4 + 1] = fmaf(-a4.y, xs, x[4 * i4 + 1]);
+                    x[4 * i4 + 2] = fmaf(-a4.z, xs, x[4 * i4 + 2]);
+                    x[4 * i4 + 3] = fmaf(-a4.w, xs, x[4 * i4 + 3]);
                 }
             }
+            // V'^T tile row vc: this thread's tokens 2 i + r
 #pragma unroll
-            for (int j = 0; j < kC / 8; ++j)
-                *reinterpret_cast<uint4*>(sm + kTileV + swz_chunk(vc, j, 128)) = pack8(x + 8 * j);
-        } else {
-            const float gamma = ms.gamma;
-            for (int v0 = 0; v0 < kV; v0 += 32) {
-                float x[32];
-                tm_ld32(tS + lanes + v0, x);
-#pragma unroll
-                for (int u = 0; u < 32; ++u) x[u] *= gamma;
-                tm_st32(tS + lanes + v0, x);
-            }
+            for (int i2 = 0; i2 < 32; ++i2)
+                *reinterpret_cast<__nv_bfloat16*>(sm + kTileV + swz(vc, 2 * i2 + r, 128)) = __float2bfloat16_rn(x[i2]);
         }
         sync_for_mma();
 
-        // ---- Z = R~ V',  S += K~^T V' ----
+        // ---- MMA 2: O += R~ V',  S^T += V'^T K~ ----
         if (tid == 0) {
-            gemm(tZ, sbase + kTileR, 128, sbase + kTileV, 128, 128, kC, false);
-            gemm(tS, sbase + kTileKd, 128, sbase + kTileV, 128, 128, kC, true);
+            gemm(tO, sbase + kTileR, 128, sbase + kTileV, 128, 128, kC, true);
+            gemm(tS, sbase + kTileV, 128, sbase + kTileKd, 128, 128, kC, true);
             commit(bar);
         }
         ok = !__syncthreads_or(!wait_parity(bar, phase));
@@ -570,56 +595,78 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_chunked_kernel(const 
         if (!ok) break;
         fence_after();
 
-        // ---- outputs (warps 0, 1: rows t < 64); next S^T image (warps 4-7) ----
-        if (warp < 2) {
-            const int t = warp * 32 + lane;
-            const float eG = ms.eG[t];
-            float rinv = 1.0f;
-            if (gated) {
-                float ss = 0.f;
-                for (int v0 = 0; v0 < kV; v0 += 32) {
-                    float y[32], z[32];
-                    tm_ld32(tY + lanes + v0, y);
-                    tm_ld32(tZ + lanes + v0, z);
+        // ---- phase 4: outputs (rows t < 64 on warps 0, 1, 4, 5; each warp half of
+        //      the columns), then the bf16 image of S^T for the next chunk ----
+        if (quad < 2 && gated) {
+            float ss = 0.f;
 #pragma unroll
-                    for (int u = 0; u < 32; ++u) {
-                        const float o = fmaf(eG, y[u], z[u]);
-                        ss = fmaf(o, o, ss);
+            for (int c = 0; c < 2; ++c) {
+                float x[32];
+                tm_ld32(tO + lanes + 64 * half + 32 * c, x);
+#pragma unroll
+                for (int u = 0; u < 32; ++u) ss = fmaf(x[u], x[u], ss);
+            }
+            ms.ssq[half][row] = ss;
+        }
+        const bool more = c0 + kC < L;
+        if (more && quad >= 2) {
+            // image rows v = 64..127 while the others wait for the norms
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                const int kd0 = 64 * half + 32 * c;
+                float x[32];
+                tm_ld32(tS + lanes + kd0, x);
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    *reinterpret_cast<uint4*>(sm + kTileS + swz_chunk(row, (kd0 >> 3) + j, 128)) = pack8(x + 8 * j);
+            }
+        }
+        __syncthreads();
+        if (quad < 2) {
+            const int t = row;
+            const bool live = t < n;                            // the TMEM loads stay warp-wide
+            const float rinv = gated ? rsqrtf((ms.ssq[0][t] + ms.ssq[1][t]) * (1.0f / kV) + p.eps) : 1.0f;
+            __nv_bfloat16* orow = live ? p.out + ms.row[t] * p.out_stride + h * kV + 64 * half : nullptr;
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                float x[32];
+                uint2 zq[8], wq[8];
+                if (gated) {
+                    // every shared load of the block before the first global store
+#pragma unroll
+                    for (int j4 = 0; j4 < 8; ++j4) {
+                        zq[j4] = Zq[t * kZStride + 16 * half + 8 * c + j4];
+                        wq[j4] = ms.w[16 * half + 8 * c + j4];
                     }
                 }
-                rinv = rsqrtf(ss * (1.0f / kV) + p.eps);
-            }
-            const bool live = t < n;
-            __nv_bfloat16* orow = live ? p.out + ms.row[t] * p.out_stride + h * kV : nullptr;
-            for (int v0 = 0; v0 < kV; v0 += 32) {
-                float y[32], z[32];
-                tm_ld32(tY + lanes + v0, y);
-                tm_ld32(tZ + lanes + v0, z);
-                if (!live) continue;
+                tm_ld32(tO + lanes + 64 * half + 32 * c, x);
 #pragma unroll
                 for (int j4 = 0; j4 < 8; ++j4) {
-                    float o[4];
+                    float y[4];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) o[e] = fmaf(eG, y[4 * j4 + e], z[4 * j4 + e]);
+                    for (int e = 0; e < 4; ++e) y[e] = x[4 * j4 + e];
                     if (gated) {
                         float zz[4], ww[4];
-                        unpack4(Zq[t * kZStride + (v0 >> 2) + j4], zz);
-                        unpack4(ms.w[(v0 >> 2) + j4], ww);
+                        unpack4(zq[j4], zz);
+                        unpack4(wq[j4], ww);
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) o[e] = o[e] * rinv * ww[e] * (zz[e] / (1.0f + expf(-zz[e])));
+                        for (int e = 0; e < 4; ++e) y[e] = y[e] * rinv * ww[e] * silu(zz[e]);
                     }
-                    *reinterpret_cast<uint2*>(orow + v0 + 4 * j4) =
-                        make_uint2(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]));
+                    if (live)
+                        *reinterpret_cast<uint2*>(orow + 32 * c + 4 * j4) =
+                            make_uint2(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]));
                 }
             }
-        } else if (warp >= 4 && c0 + kC < L) {
-            const int kd = quad * 32 + lane;
-            for (int v0 = 0; v0 < kV; v0 += 32) {
-                float x[32];
-                tm_ld32(tS + lanes + v0, x);
+            if (more) {
 #pragma unroll
-                for (int u = 0; u < 32; ++u)
-                    *reinterpret_cast<__nv_bfloat16*>(sm + kTileS + swz(v0 + u, kd, 128)) = __float2bfloat16_rn(x[u]);
+                for (int c = 0; c < 2; ++c) {
+                    const int kd0 = 64 * half + 32 * c;
+                    float x[32];
+                    tm_ld32(tS + lanes + kd0, x);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        *reinterpret_cast<uint4*>(sm + kTileS + swz_chunk(row, (kd0 >> 3) + j, 128)) = pack8(x + 8 * j);
+                }
             }
         }
         fence_before();
@@ -628,13 +675,15 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_chunked_kernel(const 
     }
 
     // ---- the final state to its slot (rounded once), then release TMEM ----
-    if (ok && wsl >= 0 && warp >= 4) {
-        const int kd = quad * 32 + lane;
-        StateT* dst = static_cast<StateT*>(p.pool) + ((wsl * p.H_v + h) * kK + kd) * static_cast<int64_t>(kV);
-        for (int v0 = 0; v0 < kV; v0 += 32) {
+    if (ok && wsl >= 0) {
+        StateT* dst = static_cast<StateT*>(p.pool) + (wsl * p.H_v + h) * static_cast<int64_t>(kK * kV) + row;
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+            const int kd0 = 64 * half + 32 * c;
             float x[32];
-            tm_ld32(tS + lanes + v0, x);
-            RowIO<StateT>::store(dst + v0, x);
+            tm_ld32(tS + lanes + kd0, x);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) store_elem(dst + (kd0 + j) * kV, x[j]);
         }
     }
     if (!ok) {
