@@ -74,8 +74,10 @@ constexpr int kA2Row = 2 * kA2Half;
 constexpr int kA2 = kTileKd + 16384;            // A     fp32 [64 s][2 parity][36 (t/2)]
 constexpr int kBStride = kC + 1;                // odd row pitch: column walks are conflict-free
 constexpr int kBT = kA2 + kC * kA2Row * 4;      // B^T   fp32 [128 v][65]
-constexpr int kZStride = kV / 4 + 1;            // uint2 per padded z row
-constexpr int kZ = kBT + kV * kBStride * 4;     // z     bf16 quads [64 t][33]
+constexpr int kStagePitch = kV / 4 + 1;         // uint2 per padded output-staging row (aliases B^T)
+static_assert(kC * kStagePitch * 8 <= kV * kBStride * 4, "staging fits the B^T region");
+constexpr int kZStride = kV / 4 + 1;            // uint2 per padded gate row
+constexpr int kZ = kBT + kV * kBStride * 4;     // w silu(z), bf16 quads [64 t][33]
 constexpr int kMisc = kZ + kC * kZStride * 8;
 
 struct Misc {
@@ -85,7 +87,6 @@ struct Misc {
     float g[kC], G[kC], beta[kC], eG[kC], kfac[kC];   // G 16-byte aligned (float4 reads)
     float ssq[2][kC];                           // per-row sums of squares of the two column halves
     int row[kC];
-    uint2 w[kV / 4];                            // norm weight, bf16 quads
 };
 static_assert(kMisc % 16 == 0 && offsetof(Misc, G) % 16 == 0, "float4 reads of G");
 constexpr int kSmemBytes = kMisc + static_cast<int>(sizeof(Misc)) + 1024;   // + base alignment slack
@@ -246,8 +247,20 @@ __device__ __forceinline__ void load_decays(const float* G, float Gt, float (&d)
     }
 }
 
-// silu(z) = z sigmoid(z); exp overflow for very negative z gives 1/inf = 0
-__device__ __forceinline__ float silu(float z) { return z * __frcp_rn(1.0f + __expf(-z)); }
+// (x0, x1) <- (a0, a1) * c + (x0, x1), one paired FP32 FMA (each lane an
+// ordinary round-to-nearest FMA)
+__device__ __forceinline__ void fma2(float& x0, float& x1, float a0, float a1, float c) {
+    uint64_t xv = (static_cast<uint64_t>(__float_as_uint(x1)) << 32) | __float_as_uint(x0);
+    const uint64_t av = (static_cast<uint64_t>(__float_as_uint(a1)) << 32) | __float_as_uint(a0);
+    const uint64_t cv = (static_cast<uint64_t>(__float_as_uint(c)) << 32) | __float_as_uint(c);
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(xv) : "l"(av), "l"(cv));
+    x0 = __uint_as_float(static_cast<uint32_t>(xv));
+    x1 = __uint_as_float(static_cast<uint32_t>(xv >> 32));
+}
+
+// silu(z) = z sigmoid(z); for very negative z the denominator overflows and
+// the fast division returns zero
+__device__ __forceinline__ float silu(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
 
 // ---- the kernel -------------------------------------------------------------------------
 //
@@ -279,6 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_chunked_kernel(const 
     float* A2 = reinterpret_cast<float*>(sm + kA2);
     float* BT = reinterpret_cast<float*>(sm + kBT);
     uint2* Zq = reinterpret_cast<uint2*>(sm + kZ);
+    uint2* Stage = reinterpret_cast<uint2*>(sm + kBT);          // output rows, after the solve
     const uint32_t sbase = saddr(sm);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quad = warp & 3;                                  // TMEM lane quadrant of this warp
@@ -314,7 +328,6 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_chunked_kernel(const 
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(saddr(&ms.bar)));
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (gated && warp == 1) ms.w[lane] = __ldg(reinterpret_cast<const uint2*>(p.norm_w) + lane);
     // rows 64-127 of the token-row tiles are zero for the whole prompt
     for (int e = tid; e < 64 * 16; e += kThreads) {
         const int r = 64 + (e >> 4), j = e & 15;
@@ -351,23 +364,24 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_chunked_kernel(const 
         }
     }
 
-    for (int c0 = 0; c0 < L; c0 += kC) {
-        const int n = min(kC, L - c0);
-
-        // ---- phase 1: per token (8 per warp) k^, q^ (bf16 tiles), v (B^T), z, gates.
-        //      Every global load of the chunk is issued before any is used; v is
-        //      read one element per lane per load (v = lane + 32 e) so that its
-        //      transposed store into B^T hits 32 distinct banks. ----
-        uint2 qraw[8], kraw[8], zraw[8];
-        __nv_bfloat16 vraw[8][4];
+    // Raw inputs of a chunk, 8 tokens per warp: q, k, z rows as bf16 quads, v one
+    // element per lane per load (v = lane + 32 e, so that its transposed store
+    // into B^T hits 32 distinct banks), a / b in lanes 0-15.  The next chunk's
+    // loads are issued as soon as the current chunk's solve has finished, so
+    // their latency overlaps the epilogue.
+    uint2 qraw[8], kraw[8], zraw[8];
+    __nv_bfloat16 vraw[8][4];
+    float ab;                                                   // lane j: a of token j, lane 8 + j: its b
+    auto load_chunk = [&](int cs) {
+        const int nn = min(kC, L - cs);
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             const int t = warp + 8 * j;
             qraw[j] = kraw[j] = zraw[j] = make_uint2(0, 0);
 #pragma unroll
             for (int e = 0; e < 4; ++e) vraw[j][e] = __float2bfloat16_rn(0.f);
-            if (t < n) {
-                const int64_t r = bos + c0 + t;
+            if (t < nn) {
+                const int64_t r = bos + cs + t;
                 qraw[j] = __ldg(reinterpret_cast<const uint2*>(p.q + r * p.q_stride + kh * kK) + lane);
                 kraw[j] = __ldg(reinterpret_cast<const uint2*>(p.k + r * p.k_stride + kh * kK) + lane);
 #pragma unroll
@@ -375,11 +389,21 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_chunked_kernel(const 
                 if (gated) zraw[j] = __ldg(reinterpret_cast<const uint2*>(p.z + r * p.z_stride + h * kV) + lane);
             }
         }
-        float ab = 0.f;                                         // lane j: a of token j, lane 8 + j: its b
-        if (lane < 16 && warp + 8 * (lane & 7) < n) {
-            const int64_t r = bos + c0 + warp + 8 * (lane & 7);
+        ab = 0.f;
+        if (lane < 16 && warp + 8 * (lane & 7) < nn) {
+            const int64_t r = bos + cs + warp + 8 * (lane & 7);
             ab = __bfloat162float(lane < 8 ? p.a[r * p.a_stride + h] : p.b[r * p.b_stride + h]);
         }
+    };
+    load_chunk(0);
+    float wv[4] = {0.f, 0.f, 0.f, 0.f};                          // this lane's 4 norm weights
+    if (gated) unpack4(__ldg(reinterpret_cast<const uint2*>(p.norm_w) + lane), wv);
+
+    for (int c0 = 0; c0 < L; c0 += kC) {
+        const int n = min(kC, L - c0);
+
+        // ---- phase 1: per token (8 per warp) k^, q^ (bf16 tiles), v (B^T), z, gates,
+        //      from the raw rows loaded while the previous chunk finished ----
         {
             // gates of the warp's 8 tokens, one per lane
             const float b_in = __shfl_down_sync(0xffffffffu, ab, 8);
@@ -419,7 +443,13 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_chunked_kernel(const 
                 float qv[4], kv[4];
                 unpack4(qraw[j], qv);
                 unpack4(kraw[j], kv);
-                if (gated) Zq[t * kZStride + lane] = zraw[j];
+                if (gated) {
+                    // the output gate w silu(z) of this lane's 4 columns, kept as bf16
+                    float zz[4];
+                    unpack4(zraw[j], zz);
+                    Zq[t * kZStride + lane] = make_uint2(pack_bf16x2(wv[0] * silu(zz[0]), wv[1] * silu(zz[1])),
+                                                         pack_bf16x2(wv[2] * silu(zz[2]), wv[3] * silu(zz[3])));
+                }
                 const float rq = rsqrtf(sums[j] + kQkEps) * p.scale;
                 const float rk = rsqrtf(sums[8 + j] + kQkEps);
                 kk = make_uint2(pack_bf16x2(kv[0] * rk, kv[1] * rk), pack_bf16x2(kv[2] * rk, kv[3] * rk));
@@ -567,14 +597,12 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_chunked_kernel(const 
 #pragma unroll
             for (int s = 0; s < kC - 1; ++s) {
                 const float mine = (r == (s & 1)) ? x[s >> 1] : 0.f;
-                const float xs = __shfl_sync(0xffffffffu, mine, (lane & ~1) | (s & 1));
+                const float nxs = -__shfl_sync(0xffffffffu, mine, (lane & ~1) | (s & 1));
 #pragma unroll
                 for (int i4 = (s >> 3); i4 < 8; ++i4) {
                     const float4 a4 = *reinterpret_cast<const float4*>(arow + s * kA2Row + 4 * i4);
-                    x[4 * i4 + 0] = fmaf(-a4.x, xs, x[4 * i4 + 0]);
-                    x[4 * i4 + 1] = fmaf(-a4.y, xs, x[4 * i4 + 1]);
-                    x[4 * i4 + 2] = fmaf(-a4.z, xs, x[4 * i4 + 2]);
-                    x[4 * i4 + 3] = fmaf(-a4.w, xs, x[4 * i4 + 3]);
+                    fma2(x[4 * i4 + 0], x[4 * i4 + 1], a4.x, a4.y, nxs);
+                    fma2(x[4 * i4 + 2], x[4 * i4 + 3], a4.z, a4.w, nxs);
                 }
             }
             // V'^T tile row vc: this thread's tokens 2 i + r
@@ -584,12 +612,13 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_chunked_kernel(const 
         }
         sync_for_mma();
 
-        // ---- MMA 2: O += R~ V',  S^T += V'^T K~ ----
+        // ---- MMA 2: O += R~ V',  S^T += V'^T K~; meanwhile the next chunk's loads ----
         if (tid == 0) {
             gemm(tO, sbase + kTileR, 128, sbase + kTileV, 128, 128, kC, true);
             gemm(tS, sbase + kTileV, 128, sbase + kTileKd, 128, 128, kC, true);
             commit(bar);
         }
+        if (c0 + kC < L) load_chunk(c0 + kC);
         ok = !__syncthreads_or(!wait_parity(bar, phase));
         phase ^= 1;
         if (!ok) break;
@@ -623,21 +652,18 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_chunked_kernel(const 
         }
         __syncthreads();
         if (quad < 2) {
+            // normalised, gated rows into the staging buffer (the B^T region,
+            // free until the next chunk), then the image rows v = 0..63
             const int t = row;
-            const bool live = t < n;                            // the TMEM loads stay warp-wide
             const float rinv = gated ? rsqrtf((ms.ssq[0][t] + ms.ssq[1][t]) * (1.0f / kV) + p.eps) : 1.0f;
-            __nv_bfloat16* orow = live ? p.out + ms.row[t] * p.out_stride + h * kV + 64 * half : nullptr;
+            uint2* srow = Stage + t * kStagePitch + 16 * half;
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
                 float x[32];
-                uint2 zq[8], wq[8];
+                uint2 gq[8];
                 if (gated) {
-                    // every shared load of the block before the first global store
 #pragma unroll
-                    for (int j4 = 0; j4 < 8; ++j4) {
-                        zq[j4] = Zq[t * kZStride + 16 * half + 8 * c + j4];
-                        wq[j4] = ms.w[16 * half + 8 * c + j4];
-                    }
+                    for (int j4 = 0; j4 < 8; ++j4) gq[j4] = Zq[t * kZStride + 16 * half + 8 * c + j4];
                 }
                 tm_ld32(tO + lanes + 64 * half + 32 * c, x);
 #pragma unroll
@@ -646,15 +672,12 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_chunked_kernel(const 
 #pragma unroll
                     for (int e = 0; e < 4; ++e) y[e] = x[4 * j4 + e];
                     if (gated) {
-                        float zz[4], ww[4];
-                        unpack4(zq[j4], zz);
-                        unpack4(wq[j4], ww);
+                        float gg[4];
+                        unpack4(gq[j4], gg);
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) y[e] = y[e] * rinv * ww[e] * silu(zz[e]);
+                        for (int e = 0; e < 4; ++e) y[e] = y[e] * rinv * gg[e];
                     }
-                    if (live)
-                        *reinterpret_cast<uint2*>(orow + 32 * c + 4 * j4) =
-                            make_uint2(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]));
+                    srow[8 * c + j4] = make_uint2(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]));
                 }
             }
             if (more) {
@@ -668,6 +691,15 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_chunked_kernel(const 
                         *reinterpret_cast<uint4*>(sm + kTileS + swz_chunk(row, (kd0 >> 3) + j, 128)) = pack8(x + 8 * j);
                 }
             }
+        }
+        __syncthreads();
+        // the chunk's output rows, one warp per 256-byte row segment
+#pragma unroll
+        for (int e = tid; e < kC * (kV / 4); e += kThreads) {
+            const int t = e >> 5, q4 = e & 31;
+            if (t < n)
+                *reinterpret_cast<uint2*>(p.out + ms.row[t] * p.out_stride + h * kV + 4 * q4) =
+                    Stage[t * kStagePitch + q4];
         }
         fence_before();
         __syncthreads();
