@@ -387,3 +387,50 @@ def token_head_updates(case: Case) -> int:
         if ql[i] > 0 and 0 <= rs[i] < case.num_slots:
             n += int(ql[i])
     return n * case.H_v
+
+
+# ---- inputs of the short causal convolution in front of the step ----------
+
+
+@dataclasses.dataclass
+class ConvInputs:
+    """Pre-convolution projection rows and conv state for a Case.
+
+    x          [num_tokens, conv_dim]              bf16 bits, channels q | k | v
+    weight     [conv_dim, width]                   bf16 bits
+    bias       [conv_dim]                          bf16 bits, or None
+    pool       [num_conv_slots, state_len, conv_dim] bf16 bits
+    conv_in, conv_out  [batch]                     int32, disjoint sets of slots
+    """
+    width: int
+    state_len: int
+    x: np.ndarray
+    weight: np.ndarray
+    bias: np.ndarray | None
+    pool: np.ndarray
+    conv_in: np.ndarray
+    conv_out: np.ndarray
+
+    @property
+    def conv_dim(self) -> int:
+        return int(self.x.shape[1])
+
+
+def conv_inputs(case: Case, width: int = 4, num_conv_slots: int | None = None, with_bias: bool = True,
+                seed: int = 0) -> ConvInputs:
+    """x ~ N(0, 1), weight ~ N(0, 0.5), bias ~ N(0, 0.1), conv-state rows
+    ~ N(0, 1), all bf16; state_len = width - 1 + spec_stride; read and write
+    slots drawn without replacement (read slots first)."""
+    rng = np.random.default_rng([seed, 3])
+    D = 2 * case.H_k * case.K + case.H_v * case.V
+    ns = num_conv_slots if num_conv_slots is not None else max(2 * case.batch, 2)
+    if ns < 2 * case.batch:
+        raise ValueError("need two conv slots per sequence")
+    state_len = width - 1 + case.spec_stride
+    x = _bf16(rng, (case.num_tokens, D))
+    weight = _bf16(rng, (D, width), 0.0, 0.5)
+    bias = _bf16(rng, (D,), 0.0, 0.1) if with_bias else None
+    pool = _bf16(rng, (ns, state_len, D))
+    perm = rng.permutation(ns).astype(np.int32)
+    return ConvInputs(width=width, state_len=state_len, x=x, weight=weight, bias=bias, pool=pool,
+                      conv_in=perm[:case.batch].copy(), conv_out=perm[case.batch:2 * case.batch].copy())

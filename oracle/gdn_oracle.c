@@ -201,6 +201,9 @@ typedef struct {
     uint16_t *out_bf16;           /* [N, H_v, V] or NULL */
     double *states_f64;           /* [batch, H_v, states_T, K, V] or NULL */
     int64_t states_T;
+    /* FP64 q, k, v (same layouts as q, k, v), used in their place when set:
+       the output of the convolution below */
+    const double *q64, *k64, *v64;
 } gdn_oracle_problem;
 
 enum {
@@ -310,6 +313,11 @@ static int check_contract(const gdn_oracle_problem* p)
 /* the step                                                                  */
 /* ------------------------------------------------------------------------- */
 
+/* q, k, v element `off` of their dense layouts, from the FP64 copy when given */
+static double in_q(const gdn_oracle_problem* p, int64_t off) { return p->q64 ? p->q64[off] : bf16_value(p->q[off]); }
+static double in_k(const gdn_oracle_problem* p, int64_t off) { return p->k64 ? p->k64[off] : bf16_value(p->k[off]); }
+static double in_v(const gdn_oracle_problem* p, int64_t off) { return p->v64 ? p->v64[off] : bf16_value(p->v[off]); }
+
 static double softplus(double x, double threshold)
 {
     return x > threshold ? x : log1p(exp(x));
@@ -333,18 +341,17 @@ static void token_step(const gdn_oracle_problem* p, int64_t r, int64_t h,
     double beta = sigmoid(bf16_value(p->b[r * H_v + h]));
 
     /* L2-normalised key and query; the query also takes the scale */
-    const uint16_t* kr = p->k + (r * p->H_k + kh) * K;
-    const uint16_t* qr = p->q + (r * p->H_k + kh) * K;
+    const int64_t kbase = (r * p->H_k + kh) * K;
     double sk = 0.0, sq = 0.0;
     for (int64_t i = 0; i < K; ++i) {
-        double kv = bf16_value(kr[i]), qv = bf16_value(qr[i]);
+        double kv = in_k(p, kbase + i), qv = in_q(p, kbase + i);
         sk += kv * kv;
         sq += qv * qv;
     }
     double rk = 1.0 / sqrt(sk + p->qk_eps), rq = 1.0 / sqrt(sq + p->qk_eps);
     for (int64_t i = 0; i < K; ++i) {
-        kn[i] = bf16_value(kr[i]) * rk;
-        qn[i] = bf16_value(qr[i]) * rq * p->scale;
+        kn[i] = in_k(p, kbase + i) * rk;
+        qn[i] = in_q(p, kbase + i) * rq * p->scale;
     }
 
     /* decay */
@@ -352,11 +359,11 @@ static void token_step(const gdn_oracle_problem* p, int64_t r, int64_t h,
     for (int64_t i = 0; i < K * V; ++i) S[i] *= decay;
 
     /* delta rule: v' = beta (v - S^T k^), then S += k^ v'^T */
-    const uint16_t* vr = p->v + (r * H_v + h) * V;
+    const int64_t vbase = (r * H_v + h) * V;
     for (int64_t j = 0; j < V; ++j) {
         double u = 0.0;
         for (int64_t i = 0; i < K; ++i) u += S[i * V + j] * kn[i];
-        double vp = beta * (bf16_value(vr[j]) - u);
+        double vp = beta * (in_v(p, vbase + j) - u);
         for (int64_t i = 0; i < K; ++i) S[i * V + j] += kn[i] * vp;
     }
 
@@ -430,7 +437,7 @@ static void run_unit(const gdn_oracle_problem* p, int64_t i, int64_t h, double* 
 
 static int check_problem(const gdn_oracle_problem* p)
 {
-    if (!p || !p->q || !p->k || !p->v || !p->a || !p->b || !p->A_log || !p->dt_bias ||
+    if (!p || !(p->q || p->q64) || !(p->k || p->k64) || !(p->v || p->v64) || !p->a || !p->b || !p->A_log || !p->dt_bias ||
         !p->pool || !p->state_indices || !p->num_accepted || !p->cu_seqlens)
         return ORC_ERR_NULL;
     if ((p->z == NULL) != (p->norm_w == NULL)) return ORC_ERR_NULL;
@@ -587,4 +594,139 @@ int gdn_oracle_prefill(const gdn_oracle_problem* p, const int32_t* read_slots, c
     return ORC_OK;
 }
 
-int gdn_oracle_abi_version(void) { return 1; }
+/* ------------------------------------------------------------------------- */
+/* the short causal convolution in front of the step, with rewind           */
+/* ------------------------------------------------------------------------- */
+
+/*
+ * The projection rows that feed q, k and v pass first through a depthwise
+ * causal convolution of width W with a SiLU, whose history lives in a conv
+ * state slot ([P1] implementation step 2 and its spec-aware listing: a wide
+ * rolling buffer sliced per token, convolved, written back; [P2]
+ * implementation step 3: the speculative path runs causal_conv1d_update with
+ * rewind before the post-conv decode kernel; BF16 conv state).  The pages
+ * print no formula; the readings taken here:
+ *   - a conv slot is [state_len][conv_dim] raw inputs (bf16 bits), rows
+ *     0 .. W-2 the history before the previous step, rows W-1 .. the previous
+ *     step's own inputs;
+ *   - rewind: with a = max(num_accepted[i], 1) (the clamp mirrors the state
+ *     rewind), the W-1 inputs before this step's first token are slot rows
+ *     a .. a + W - 2, i.e. the history up to the previous step's last
+ *     accepted token;
+ *   - y_t[c] = silu(bias[c] + sum_{w<W} weight[c][w] x_{t-W+1+w}[c]) over the
+ *     inputs x (history first, then this step's rows in order);
+ *   - the new slot: rows 0 .. W-2 = that history, rows W-1 .. W-2+q_len = this
+ *     step's raw inputs, copied bit for bit; later rows are left as they were;
+ *   - a sequence reads conv_in[i] (< 0: zero history) and writes conv_out[i]
+ *     (< 0: no write), which must differ from every read slot of the call.
+ * conv_dim = 2 H_k K + H_v V with the channels in the order q | k | v.
+ */
+typedef struct {
+    int64_t conv_dim, width, state_len, num_conv_slots;
+    const uint16_t* x;            /* bf16 bits [num_tokens, conv_dim]: projection rows */
+    const uint16_t* weight;       /* bf16 bits [conv_dim, width] */
+    const uint16_t* bias;         /* bf16 bits [conv_dim], or NULL */
+    uint16_t* conv_pool;          /* bf16 bits [num_conv_slots, state_len, conv_dim] */
+    const int32_t* conv_in;       /* [batch] */
+    const int32_t* conv_out;      /* [batch] */
+} gdn_oracle_conv;
+
+/* does the step process sequence i (a token and an unpadded read slot)? */
+static int processed(const gdn_oracle_problem* p, int64_t i)
+{
+    int64_t ql = (int64_t)p->cu_seqlens[i + 1] - p->cu_seqlens[i];
+    return ql > 0 && read_index(p, i) >= 0;
+}
+
+/*
+ * The convolution for every processed sequence of the step, then the step
+ * itself on its output (q, k, v in FP64).  The step's own contract and the
+ * conv slot contract are checked first; nothing is modified on error.
+ */
+int gdn_oracle_spec_decode_conv(const gdn_oracle_problem* pin, const gdn_oracle_conv* c)
+{
+    if (!pin || !c || !c->x || !c->weight || !c->conv_pool || !c->conv_in || !c->conv_out) return ORC_ERR_NULL;
+    gdn_oracle_problem p = *pin;
+    const int64_t B = p.batch, N = p.num_tokens, W = c->width, D = c->conv_dim;
+    const int64_t QK = p.H_k * p.K;
+    if (D != 2 * QK + p.H_v * p.V || W < 1 || c->state_len < W - 1 + p.spec_stride || c->num_conv_slots <= 0)
+        return ORC_ERR_SHAPE;
+    /* the bf16 q/k/v pointers are not used: stand-ins for the null checks */
+    p.q = p.k = p.v = c->x;
+    int rc = check_problem(&p);
+    if (rc != ORC_OK) return rc;
+    rc = check_contract(&p);
+    if (rc != ORC_OK) return rc;
+    for (int64_t i = 0; i < B; ++i) {
+        if (!processed(&p, i)) continue;
+        if (c->conv_in[i] >= c->num_conv_slots || c->conv_out[i] >= c->num_conv_slots) return ORC_ERR_SLOT;
+        for (int64_t j = 0; j < B; ++j) {
+            if (!processed(&p, j) || c->conv_out[j] < 0) continue;
+            if (c->conv_out[j] == c->conv_in[i]) return ORC_ERR_CONFLICT;
+            if (j != i && c->conv_out[j] == c->conv_out[i]) return ORC_ERR_CONFLICT;
+        }
+    }
+    double* y = (double*)calloc((size_t)(N * D), sizeof(double));
+    double* q64 = (double*)calloc((size_t)(N * QK), sizeof(double));
+    double* k64 = (double*)calloc((size_t)(N * QK), sizeof(double));
+    double* v64 = (double*)calloc((size_t)(N * p.H_v * p.V), sizeof(double));
+    double* hist = (double*)malloc(sizeof(double) * (size_t)((W - 1 + p.spec_stride) * D + 1));
+    uint16_t* newslot = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)(B * (W - 1 + p.spec_stride) * D + 1));
+    if (!y || !q64 || !k64 || !v64 || !hist || !newslot) {
+        free(y); free(q64); free(k64); free(v64); free(hist); free(newslot);
+        return ORC_ERR_NOMEM;
+    }
+    const int64_t rows_new = W - 1 + p.spec_stride;
+    for (int64_t i = 0; i < B; ++i) {
+        if (!processed(&p, i)) continue;
+        const int64_t ql = (int64_t)p.cu_seqlens[i + 1] - p.cu_seqlens[i];
+        const int64_t acc = p.num_accepted[i] > 1 ? p.num_accepted[i] : 1;
+        /* inputs in time order: W-1 history rows, then the step's rows */
+        for (int64_t m = 0; m < W - 1; ++m)
+            for (int64_t ch = 0; ch < D; ++ch) {
+                uint16_t bits = 0;
+                if (c->conv_in[i] >= 0)
+                    bits = c->conv_pool[((int64_t)c->conv_in[i] * c->state_len + acc + m) * D + ch];
+                hist[m * D + ch] = bf16_value(bits);
+                newslot[(i * rows_new + m) * D + ch] = bits;
+            }
+        for (int64_t t = 0; t < ql; ++t) {
+            const int64_t r = token_row(&p, i, t);
+            for (int64_t ch = 0; ch < D; ++ch) {
+                hist[(W - 1 + t) * D + ch] = bf16_value(c->x[r * D + ch]);
+                newslot[(i * rows_new + W - 1 + t) * D + ch] = c->x[r * D + ch];
+            }
+        }
+        for (int64_t t = 0; t < ql; ++t) {
+            const int64_t r = token_row(&p, i, t);
+            for (int64_t ch = 0; ch < D; ++ch) {
+                double acc_c = c->bias ? bf16_value(c->bias[ch]) : 0.0;
+                for (int64_t w = 0; w < W; ++w)
+                    acc_c += bf16_value(c->weight[ch * W + w]) * hist[(t + w) * D + ch];
+                y[r * D + ch] = acc_c / (1.0 + exp(-acc_c));          /* SiLU */
+            }
+        }
+    }
+    /* all reads done: write the new slots */
+    for (int64_t i = 0; i < B; ++i) {
+        if (!processed(&p, i) || c->conv_out[i] < 0) continue;
+        const int64_t ql = (int64_t)p.cu_seqlens[i + 1] - p.cu_seqlens[i];
+        for (int64_t m = 0; m < W - 1 + ql; ++m)
+            memcpy(c->conv_pool + ((int64_t)c->conv_out[i] * c->state_len + m) * D,
+                   newslot + (i * rows_new + m) * D, sizeof(uint16_t) * (size_t)D);
+    }
+    /* split the conv output into the step's q, k, v layouts */
+    for (int64_t r = 0; r < N; ++r) {
+        memcpy(q64 + r * QK, y + r * D, sizeof(double) * (size_t)QK);
+        memcpy(k64 + r * QK, y + r * D + QK, sizeof(double) * (size_t)QK);
+        memcpy(v64 + r * p.H_v * p.V, y + r * D + 2 * QK, sizeof(double) * (size_t)(p.H_v * p.V));
+    }
+    p.q64 = q64;
+    p.k64 = k64;
+    p.v64 = v64;
+    rc = gdn_oracle_spec_decode(&p);
+    free(y); free(q64); free(k64); free(v64); free(hist); free(newslot);
+    return rc;
+}
+
+int gdn_oracle_abi_version(void) { return 2; }

@@ -70,6 +70,17 @@ class Problem(ctypes.Structure):
         ("pool", ctypes.c_void_p),
         ("out_f64", ctypes.c_void_p), ("out_bf16", ctypes.c_void_p),
         ("states_f64", ctypes.c_void_p), ("states_T", ctypes.c_int64),
+        ("q64", ctypes.c_void_p), ("k64", ctypes.c_void_p), ("v64", ctypes.c_void_p),
+    ]
+
+
+class Conv(ctypes.Structure):
+    """Mirror of gdn_oracle_conv."""
+    _fields_ = [
+        ("conv_dim", ctypes.c_int64), ("width", ctypes.c_int64),
+        ("state_len", ctypes.c_int64), ("num_conv_slots", ctypes.c_int64),
+        ("x", ctypes.c_void_p), ("weight", ctypes.c_void_p), ("bias", ctypes.c_void_p),
+        ("conv_pool", ctypes.c_void_p), ("conv_in", ctypes.c_void_p), ("conv_out", ctypes.c_void_p),
     ]
 
 
@@ -84,6 +95,8 @@ def load() -> ctypes.CDLL:
             lib.gdn_oracle_decode_nonspec.restype = ctypes.c_int
             lib.gdn_oracle_prefill.argtypes = [ctypes.POINTER(Problem), ctypes.c_void_p, ctypes.c_void_p]
             lib.gdn_oracle_prefill.restype = ctypes.c_int
+            lib.gdn_oracle_spec_decode_conv.argtypes = [ctypes.POINTER(Problem), ctypes.POINTER(Conv)]
+            lib.gdn_oracle_spec_decode_conv.restype = ctypes.c_int
             for name in ("gdn_oracle_round_bf16", "gdn_oracle_round_f16", "gdn_oracle_round_f32",
                          "gdn_oracle_value_bf16", "gdn_oracle_value_f16"):
                 getattr(lib, name).argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64]
@@ -257,3 +270,48 @@ def run_case(case, pool, **kw):
         state_indices=case.state_indices, num_accepted=case.num_accepted,
         cu_seqlens=case.cu_seqlens, spec_token_indx=case.spec_token_indx,
         num_tokens=case.num_tokens, scale=case.scale, eps=case.eps, **kw)
+
+
+def spec_decode_conv(*, x, conv_weight, conv_bias, conv_pool, conv_in, conv_out, H_k, K, a, b, z, A_log,
+                     dt_bias, norm_w, pool, state_dtype, state_indices, num_accepted, cu_seqlens,
+                     spec_token_indx=None, scale=128 ** -0.5, eps=1e-5, qk_eps=1e-6,
+                     softplus_threshold=20.0, num_threads=1):
+    """The short causal convolution with rewind, then the step on its output
+    (see ``gdn_oracle_spec_decode_conv``).  ``x`` [num_tokens, conv_dim] are the
+    projection rows (bf16 bits, channels q | k | v); ``conv_weight``
+    [conv_dim, width], ``conv_bias`` [conv_dim] or None; ``conv_pool``
+    [num_conv_slots, state_len, conv_dim] bf16 bits, updated in place, like
+    ``pool``.  Returns out_f64 / out_bf16 as ``spec_decode`` does."""
+    lib = load()
+    x = _c(x, np.uint16); w = _c(conv_weight, np.uint16); cb = _c(conv_bias, np.uint16)
+    a = _c(a, np.uint16); b = _c(b, np.uint16); z = _c(z, np.uint16)
+    A_log = _c(A_log, np.float32); dt_bias = _c(dt_bias, np.uint16); norm_w = _c(norm_w, np.uint16)
+    idx = _c(state_indices, np.int32); acc = _c(num_accepted, np.int32)
+    cu = _c(cu_seqlens, np.int32); sti = _c(spec_token_indx, np.int32)
+    cin = _c(conv_in, np.int32); cout = _c(conv_out, np.int32)
+    if pool.dtype != _POOL_DTYPES[state_dtype] or not pool.flags.c_contiguous:
+        raise TypeError("pool must be a contiguous array of the state dtype's storage type")
+    if conv_pool.dtype != np.uint16 or not conv_pool.flags.c_contiguous:
+        raise TypeError("conv_pool must be a contiguous uint16 (bf16 bits) array")
+    N, D = x.shape
+    H_v, V = a.shape[1], pool.shape[3]
+    batch, stride = idx.shape
+    out_f64 = np.full((N, H_v, V), np.nan)
+    out_bf16 = np.full((N, H_v, V), 0xFFFF, dtype=np.uint16)
+    p = Problem(
+        batch=batch, num_tokens=N, H_k=H_k, H_v=H_v, K=K, V=V, spec_stride=stride,
+        num_slots=pool.shape[0], state_dtype=state_dtype, num_threads=num_threads,
+        scale=scale, eps=eps, qk_eps=qk_eps, softplus_threshold=softplus_threshold,
+        a=_ptr(a), b=_ptr(b), z=_ptr(z),
+        A_log=_ptr(A_log), dt_bias=_ptr(dt_bias), norm_w=_ptr(norm_w),
+        state_indices=_ptr(idx), num_accepted=_ptr(acc), cu_seqlens=_ptr(cu),
+        spec_token_indx=_ptr(sti), pool=pool.ctypes.data,
+        out_f64=out_f64.ctypes.data, out_bf16=out_bf16.ctypes.data,
+    )
+    c = Conv(conv_dim=D, width=w.shape[1], state_len=conv_pool.shape[1], num_conv_slots=conv_pool.shape[0],
+             x=_ptr(x), weight=_ptr(w), bias=_ptr(cb), conv_pool=conv_pool.ctypes.data,
+             conv_in=_ptr(cin), conv_out=_ptr(cout))
+    rc = lib.gdn_oracle_spec_decode_conv(ctypes.byref(p), ctypes.byref(c))
+    if rc != 0:
+        raise OracleError(f"oracle rejected the problem: {ERRORS.get(rc, rc)}")
+    return {"out_f64": out_f64, "out_bf16": out_bf16}
