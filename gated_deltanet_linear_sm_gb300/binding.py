@@ -40,6 +40,16 @@ class gdn_dims(ctypes.Structure):
     ]
 
 
+class gdn_conv_dims(ctypes.Structure):
+    """Mirror of gdn_conv_dims in include/gdnspec.h."""
+
+    _fields_ = [
+        ("width", ctypes.c_int32), ("state_len", ctypes.c_int32),
+        ("num_conv_slots", ctypes.c_int64), ("x_stride", ctypes.c_int64),
+        ("reserved", ctypes.c_int32 * 2),
+    ]
+
+
 class GdnError(RuntimeError):
     def __init__(self, status: int, text: str):
         super().__init__(f"gdn_spec_decode failed: {text} (status {status})")
@@ -62,6 +72,8 @@ EXPORTS = {
                                                ctypes.c_int, _VP, _VP]),
     "gdn_prefill_chunked": (ctypes.c_int, [_VP] * 14 + [ctypes.POINTER(gdn_dims), ctypes.c_float,
                                                        ctypes.c_float, ctypes.c_int, _VP, _VP]),
+    "gdn_spec_decode_conv": (ctypes.c_int, [_VP] * 6 + [ctypes.POINTER(gdn_conv_dims)] + [_VP] * 12 +
+                             [ctypes.POINTER(gdn_dims), ctypes.c_float, ctypes.c_float, ctypes.c_int, _VP, _VP]),
     "gdn_spec_decode_split": (ctypes.c_int32, [ctypes.POINTER(gdn_dims)]),
     "gdn_status_str": (ctypes.c_char_p, [ctypes.c_int]),
     "gdn_version": (ctypes.c_int32, []),
@@ -307,6 +319,78 @@ def _prefill(entry, q, k, v, a, b, z, A_log, dt_bias, norm_w, state_pool, read_s
         _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(b), _ptr(z), _ptr(A_log), _ptr(dt_bias), _ptr(norm_w),
         _ptr(state_pool), _ptr(read_slots), _ptr(write_slots), _ptr(cu_seqlens), _ptr(out),
         ctypes.byref(dims), float(scale), float(eps), _STATE_DTYPES[state_pool.dtype], _ptr(status), handle)
+    if rc != 0:
+        raise GdnError(rc, status_str(rc))
+    return out
+
+
+def gdn_spec_decode_conv(x, conv_weight, conv_bias, conv_pool, conv_in, conv_out, a, b, z, A_log, dt_bias,
+                         norm_w, state_pool, state_indices, num_accepted, cu_seqlens, out, *, H_k, K=128,
+                         spec_token_indx=None, scale=128 ** -0.5, eps=1e-5, max_T=None, status=None,
+                         stream=None):
+    """The speculative step with the short causal convolution fused in front
+    (see include/gdnspec.h): x [N, conv_dim] bf16 projection rows (channels
+    q | k | v), conv_weight [conv_dim, W] bf16, conv_bias [conv_dim] bf16 or
+    None, conv_pool [num_conv_slots, state_len, conv_dim] bf16 (updated in
+    place), conv_in / conv_out [B] int32; the other tensors as for
+    gdn_spec_decode.  Returns ``out``."""
+    dev = x.device
+    if dev.type != "cuda":
+        raise ValueError("gdn_spec_decode_conv runs on CUDA tensors only")
+    bf = torch.bfloat16
+    for t, n in ((x, "x"), (conv_weight, "conv_weight"), (conv_pool, "conv_pool"), (a, "a"), (b, "b"),
+                 (dt_bias, "dt_bias"), (out, "out")):
+        _check(t, n, bf, dev)
+    if conv_bias is not None:
+        _check(conv_bias, "conv_bias", bf, dev)
+    if (z is None) != (norm_w is None):
+        raise ValueError("z and norm_w must both be given or both be None")
+    if z is not None:
+        _check(z, "z", bf, dev)
+        _check(norm_w, "norm_w", bf, dev)
+    _check(A_log, "A_log", torch.float32, dev)
+    for t, n in ((state_indices, "state_indices"), (num_accepted, "num_accepted"), (cu_seqlens, "cu_seqlens"),
+                 (conv_in, "conv_in"), (conv_out, "conv_out")):
+        _check(t, n, torch.int32, dev)
+        if not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous")
+    if spec_token_indx is not None:
+        _check(spec_token_indx, "spec_token_indx", torch.int32, dev)
+    if status is not None:
+        _check(status, "status", torch.int32, dev)
+    if not (conv_weight.is_contiguous() and conv_pool.is_contiguous() and
+            (conv_bias is None or conv_bias.is_contiguous())):
+        raise ValueError("conv_weight, conv_bias and conv_pool must be contiguous")
+    if x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError("x must be [N, conv_dim] with contiguous channels")
+    if state_pool.dtype not in _STATE_DTYPES or state_pool.device != dev or not state_pool.is_contiguous():
+        raise ValueError("state_pool must be a contiguous fp32 / bf16 / fp16 tensor on the same device")
+    N, D = x.shape
+    H_v, V = state_pool.shape[1], state_pool.shape[3]
+    if D != 2 * H_k * K + H_v * V or conv_weight.shape[0] != D or conv_pool.shape[2] != D:
+        raise ValueError("conv_dim must be 2 H_k K + H_v V for x, conv_weight and conv_pool")
+    d = gdn_dims()
+    d.batch, d.num_tokens, d.H_k, d.H_v, d.K, d.V = state_indices.shape[0], N, H_k, H_v, K, V
+    d.spec_stride = state_indices.shape[1]
+    d.max_T = d.spec_stride if max_T is None else max_T
+    d.num_slots = state_pool.shape[0]
+    d.a_stride = _row_stride(a, "a", H_v)
+    d.b_stride = _row_stride(b, "b", H_v)
+    d.z_stride = _row_stride(z, "z", H_v * V) if z is not None else 0
+    d.out_stride = _row_stride(out, "out", H_v * V)
+    cd = gdn_conv_dims()
+    cd.width = conv_weight.shape[1]
+    cd.state_len = conv_pool.shape[1]
+    cd.num_conv_slots = conv_pool.shape[0]
+    cd.x_stride = x.stride(0) if N > 1 else D
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else stream
+    rc = load_library().gdn_spec_decode_conv(
+        _ptr(x), _ptr(conv_weight), _ptr(conv_bias), _ptr(conv_pool), _ptr(conv_in), _ptr(conv_out),
+        ctypes.byref(cd), _ptr(a), _ptr(b), _ptr(z), _ptr(A_log), _ptr(dt_bias), _ptr(norm_w), _ptr(state_pool),
+        _ptr(state_indices), _ptr(num_accepted), _ptr(cu_seqlens), _ptr(spec_token_indx), _ptr(out),
+        ctypes.byref(d), float(scale), float(eps), _STATE_DTYPES[state_pool.dtype], _ptr(status), handle)
     if rc != 0:
         raise GdnError(rc, status_str(rc))
     return out

@@ -38,6 +38,15 @@ struct Params {
     int64_t num_slots;
     int32_t batch, num_tokens, H_k, H_v, stride, max_T, group;
     float scale, eps;
+    // short causal convolution in front of the step (gdn_spec_decode_conv only)
+    const __nv_bfloat16* x;          // pre-convolution rows, channels q | k | v
+    const __nv_bfloat16* conv_w;     // [conv_dim][width]
+    const __nv_bfloat16* conv_b;     // [conv_dim] or null
+    __nv_bfloat16* conv_pool;        // [num_conv_slots][state_len][conv_dim]
+    const int32_t* conv_in;
+    const int32_t* conv_out;
+    int64_t x_stride, num_conv_slots;
+    int32_t conv_dim, conv_width, conv_state_len;
 };
 
 // Launch the chunked prefill kernel: one CTA per (sequence, v-head) unit.

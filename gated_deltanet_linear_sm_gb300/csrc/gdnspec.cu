@@ -169,8 +169,9 @@ __device__ __forceinline__ void raise_flag(const Params& p, int rank, int flag) 
 // Per-token prologue arithmetic for token t of unit (i, h), one warp: the raw
 // quads are this lane's 4 elements of q, k (key head), v and z (v-head);
 // `ws` is the slot that receives the state after this token (-1: none).
-__device__ __forceinline__ void prologue_token(Smem& s, const Params& p, int h, int t, int r, int lane,
-                                               uint2 qraw, uint2 kraw, uint2 vraw, uint2 zraw, long long ws) {
+__device__ __forceinline__ void prologue_token_f(Smem& s, const Params& p, int h, int t, int r, int lane,
+                                                 float (&qv)[4], float (&kv)[4], const float (&vv)[4], uint2 zraw,
+                                                 long long ws) {
     float a_in = 0.f, b_in = 0.f, dtb = 0.f, alog = 0.f;
     if (lane == 0) {
         a_in = __bfloat162float(p.a[r * p.a_stride + h]);
@@ -178,10 +179,6 @@ __device__ __forceinline__ void prologue_token(Smem& s, const Params& p, int h, 
         dtb = __bfloat162float(p.dt_bias[h]);
         alog = __ldg(p.A_log + h);
     }
-    float qv[4], kv[4], vv[4];
-    unpack_bf16x4(qraw, qv);
-    unpack_bf16x4(kraw, kv);
-    unpack_bf16x4(vraw, vv);
     float sq = 0.f, sk = 0.f;
 #pragma unroll
     for (int e = 0; e < 4; ++e) { sq += qv[e] * qv[e]; sk += kv[e] * kv[e]; }
@@ -206,6 +203,15 @@ __device__ __forceinline__ void prologue_token(Smem& s, const Params& p, int h, 
         s.row[t] = r;
         s.ws[t] = ws;
     }
+}
+
+__device__ __forceinline__ void prologue_token(Smem& s, const Params& p, int h, int t, int r, int lane,
+                                               uint2 qraw, uint2 kraw, uint2 vraw, uint2 zraw, long long ws) {
+    float qv[4], kv[4], vv[4];
+    unpack_bf16x4(qraw, qv);
+    unpack_bf16x4(kraw, kv);
+    unpack_bf16x4(vraw, vv);
+    prologue_token_f(s, p, h, t, r, lane, qv, kv, vv, zraw, ws);
 }
 
 // One draft token for this lane's 16x4 block: both reductions, the delta rule,
@@ -368,11 +374,78 @@ __device__ __forceinline__ void load_token_quads(const Params& p, int r, int kh,
                           : make_uint2(0, 0);
 }
 
+// ---- the short causal convolution in front of the step ------------------------------
+
+// The three 4-channel groups of this lane in a projection row: q and k of key
+// head kh, v of v-head h (channels in the order q | k | v).
+__device__ __forceinline__ void conv_channels(const Params& p, int kh, int h, int lane, int (&ch)[3]) {
+    const int qk = p.H_k * kK;
+    ch[0] = kh * kK + lane * 4;
+    ch[1] = qk + kh * kK + lane * 4;
+    ch[2] = 2 * qk + h * kV + lane * 4;
+}
+
+// The W-1 rewound history rows of sequence i in its read slot (rows a ..
+// a+W-2, a = max(num_accepted, 1)), or null for zero history.
+__device__ __forceinline__ const __nv_bfloat16* conv_history(const Params& p, int i, int acc) {
+    const long long ci = __ldg(p.conv_in + i);
+    return ci < 0 ? nullptr
+                  : p.conv_pool + (ci * p.conv_state_len + max(acc, 1)) * static_cast<int64_t>(p.conv_dim);
+}
+
+// Row of the step's token tau of the sequence starting at bos (gathered
+// through spec_token_indx when given); -1 when out of range.
+__device__ __forceinline__ int conv_row(const Params& p, int bos, int tau) {
+    const int n = bos + tau;
+    const int r = p.sti != nullptr ? __ldg(p.sti + n) : n;
+    return (r < 0 || r >= p.num_tokens) ? -1 : r;
+}
+
+// q, k, v of draft token t for this lane's channels: y = silu(bias + sum_w
+// weight[w] x_{t-W+1+w}) over (the W-1 history rows at `hist`, null for zero
+// history; then the step's rows), FP32.  Sets `bad` for an out-of-range row.
+__device__ __forceinline__ void conv_token(const Params& p, int bos, int t, const int (&ch)[3],
+                                           const __nv_bfloat16* hist, float (&y)[3][4], int& bad) {
+    const int W = p.conv_width;
+#pragma unroll
+    for (int g = 0; g < 3; ++g) {
+        float b4[4] = {0.f, 0.f, 0.f, 0.f};
+        if (p.conv_b != nullptr) unpack_bf16x4(ldg_quad(p.conv_b + ch[g]), b4);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) y[g][e] = b4[e];
+    }
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+        if (w >= W) break;
+        const int tau = t - (W - 1) + w;
+        const __nv_bfloat16* src = nullptr;
+        if (tau < 0) {
+            if (hist != nullptr) src = hist + static_cast<int64_t>(W - 1 + tau) * p.conv_dim;
+        } else {
+            const int r = conv_row(p, bos, tau);
+            if (r < 0) bad = 1;
+            else src = p.x + r * p.x_stride;
+        }
+#pragma unroll
+        for (int g = 0; g < 3; ++g) {
+            float u[4] = {0.f, 0.f, 0.f, 0.f};
+            if (src != nullptr) unpack_bf16x4(ldg_quad(src + ch[g]), u);
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                y[g][e] = fmaf(__bfloat162float(p.conv_w[static_cast<int64_t>(ch[g] + e) * W + w]), u[e], y[g][e]);
+        }
+    }
+#pragma unroll
+    for (int g = 0; g < 3; ++g)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) y[g][e] = y[g][e] / (1.0f + expf(-y[g][e]));
+}
+
 // ---- the speculative decode kernel -------------------------------------------------
 //
 // Grid: one CTA per (unit, column slice); SPLIT CTAs of a unit form one cluster.
 // Block: 8 / SPLIT warps, each owning 16 of the unit's 128 V columns.
-template <typename StateT, int SPLIT>
+template <typename StateT, int SPLIT, bool CONV = false>
 __global__ void __launch_bounds__(Config<StateT, SPLIT>::kThreads, 2 * SPLIT)
 gdn_spec_decode_kernel(const Params p) {
     using C = Config<StateT, SPLIT>;
@@ -417,6 +490,12 @@ gdn_spec_decode_kernel(const Params p) {
     if (rj >= kMaxT) rs = __ldg(slot_row + rj);                // acceptance beyond the first 8 columns
     if (rs < 0) return;                                        // padded sequence
     if (rs >= p.num_slots) { raise_flag(p, rank, GDN_FLAG_SLOT_RANGE); return; }
+    if constexpr (CONV) {
+        if (__ldg(p.conv_in + i) >= p.num_conv_slots || __ldg(p.conv_out + i) >= p.num_conv_slots) {
+            raise_flag(p, rank, GDN_FLAG_SLOT_RANGE);
+            return;
+        }
+    }
 
     // ---- load this lane's 16x4 block of the state tile (FP32 in registers) ----
     const StateT* src = static_cast<const StateT*>(p.pool) + (rs * p.H_v + h) * kTile;
@@ -429,6 +508,7 @@ gdn_spec_decode_kernel(const Params p) {
     const int kh = h / p.group;
     if (p.z != nullptr && warp == 0) s.w[lane] = ldg_quad(p.norm_w + lane * 4);
     int bad = 0;
+
 #pragma unroll
     for (int j = 0; j < SPLIT; ++j) {                          // W * SPLIT = 8 >= q_len
         const int t = warp + j * W;
@@ -438,19 +518,59 @@ gdn_spec_decode_kernel(const Params p) {
             if (r < 0 || r >= p.num_tokens) {
                 bad = 1;
             } else {
-                uint2 qraw, kraw, vraw, zraw;
-                load_token_quads(p, r, kh, h, lane, qraw, kraw, vraw, zraw);
                 long long ws = 0;
 #pragma unroll
                 for (int jj = 0; jj < kMaxT; ++jj)
                     if (jj == t) ws = slots[jj];                   // t < q_len <= 8
-                prologue_token(s, p, h, t, r, lane, qraw, kraw, vraw, zraw, ws);
+                if constexpr (CONV) {
+                    int conv_ch[3];
+                    conv_channels(p, kh, h, lane, conv_ch);
+                    float y[3][4];
+                    conv_token(p, bos, t, conv_ch, conv_history(p, i, acc), y, bad);
+                    const uint2 zraw = p.z != nullptr
+                                           ? ldg_quad(p.z + r * p.z_stride + static_cast<int64_t>(h) * kV + lane * 4)
+                                           : make_uint2(0, 0);
+                    prologue_token_f(s, p, h, t, r, lane, y[0], y[1], y[2], zraw, ws);
+                } else {
+                    uint2 qraw, kraw, vraw, zraw;
+                    load_token_quads(p, r, kh, h, lane, qraw, kraw, vraw, zraw);
+                    prologue_token(s, p, h, t, r, lane, qraw, kraw, vraw, zraw, ws);
+                }
             }
         }
     }
     // publishes the prologue; every CTA of the cluster checks every token row,
     // so the skip decision below is the same in all of them
     if (__syncthreads_or(bad)) { raise_flag(p, rank, GDN_FLAG_TOKEN_ROW); return; }
+
+    // ---- the new conv slot: the history, then this step's rows.  Channels of
+    //      v-head h by this unit; q / k channels of the key head by its first
+    //      v-head only.  (Only with SPLIT = 1.) ----
+    if constexpr (CONV) {
+        const long long conv_out = __ldg(p.conv_out + i);
+        if (conv_out >= 0) {
+            int conv_ch[3];
+            conv_channels(p, kh, h, lane, conv_ch);
+            const __nv_bfloat16* hist = conv_history(p, i, acc);
+            __nv_bfloat16* dst = p.conv_pool + conv_out * p.conv_state_len * static_cast<int64_t>(p.conv_dim);
+            const int g0 = (h % p.group) == 0 ? 0 : 2;
+            const int Wc = p.conv_width;
+            if (warp < q_len) {
+                const int r = conv_row(p, bos, warp);
+                const __nv_bfloat16* src = p.x + r * p.x_stride;
+                for (int g = g0; g < 3; ++g)
+                    *reinterpret_cast<uint2*>(dst + static_cast<int64_t>(Wc - 1 + warp) * p.conv_dim + conv_ch[g]) =
+                        ldg_quad(src + conv_ch[g]);
+            }
+            if (warp == 0) {
+                for (int m = 0; m < Wc - 1; ++m)
+                    for (int g = g0; g < 3; ++g)
+                        *reinterpret_cast<uint2*>(dst + static_cast<int64_t>(m) * p.conv_dim + conv_ch[g]) =
+                            hist != nullptr ? ldg_quad(hist + static_cast<int64_t>(m) * p.conv_dim + conv_ch[g])
+                                            : make_uint2(0, 0);
+            }
+        }
+    }
 
     // ---- the draft tokens, in order ----
     for (int t = 0; t < q_len; ++t) token_step<StateT>(S, s, p, t, h, lane, col0, row0, rank);
@@ -525,10 +645,10 @@ __global__ void __launch_bounds__(256, 2) gdn_prefill_kernel(const Params p) {
 
 // ---- host side ----------------------------------------------------------------
 
-template <typename StateT, int SPLIT>
+template <typename StateT, int SPLIT, bool CONV = false>
 cudaError_t launch(const Params& p, int64_t units, cudaStream_t stream) {
     using C = Config<StateT, SPLIT>;
-    auto kernel = gdn_spec_decode_kernel<StateT, SPLIT>;
+    auto kernel = gdn_spec_decode_kernel<StateT, SPLIT, CONV>;
     if (C::kSmem > 48 * 1024) {
         // opt in to more than 48 KB of dynamic shared memory, once per device
         static bool done[64] = {false};
@@ -687,6 +807,11 @@ struct DecodeLauncher {
 };
 
 template <typename StateT>
+struct ConvDecodeLauncher {
+    static cudaError_t run(const Params& p, int64_t units, cudaStream_t s) { return launch<StateT, 1, true>(p, units, s); }
+};
+
+template <typename StateT>
 struct PrefillLauncher {
     static cudaError_t run(const Params& p, int64_t units, cudaStream_t s) { return launch_prefill<StateT>(p, units, s); }
 };
@@ -719,6 +844,54 @@ gdn_status gdn_spec_decode(const void* q, const void* k, const void* v, const vo
     const int split = dims->split ? dims->split : choose_split(units);
     const cudaError_t err =
         by_state_dtype<DecodeLauncher>(state_dtype, p, units, split, reinterpret_cast<cudaStream_t>(stream));
+    return err == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+gdn_status gdn_spec_decode_conv(const void* x, const void* conv_weight, const void* conv_bias, void* conv_pool,
+                                const int32_t* conv_in, const int32_t* conv_out, const gdn_conv_dims* cdims,
+                                const void* a, const void* b, const void* z, const float* A_log, const void* dt_bias,
+                                const void* norm_w, void* state_pool, const int32_t* state_indices,
+                                const int32_t* num_accepted, const int32_t* cu_seqlens,
+                                const int32_t* spec_token_indx, void* out, const gdn_dims* dims, float scale,
+                                float eps, gdn_dtype state_dtype, int32_t* status_word, gdn_stream_t stream) {
+    const gdn_status ds = check_dims(dims);
+    if (ds != GDN_OK) return ds;
+    if (cdims == nullptr) return GDN_ERR_NULL_ARG;
+    if (cdims->width < 1 || cdims->width > 4 || cdims->num_conv_slots < 1 || cdims->x_stride < 0 ||
+        cdims->reserved[0] != 0 || cdims->reserved[1] != 0 ||
+        static_cast<int64_t>(cdims->state_len) < cdims->width - 1 + static_cast<int64_t>(dims->spec_stride))
+        return GDN_ERR_BAD_SHAPE;
+    if (state_dtype != GDN_F32 && state_dtype != GDN_BF16 && state_dtype != GDN_F16) return GDN_ERR_UNSUPPORTED;
+    if (dims->split > 1) return GDN_ERR_UNSUPPORTED;
+    if (dims->batch == 0) return GDN_OK;
+    if (!state_indices || !num_accepted || !x || !conv_weight || !conv_pool || !conv_in || !conv_out)
+        return GDN_ERR_NULL_ARG;
+    Params p;
+    // q, k and v are not read on this path: x stands in for the null checks
+    const gdn_status ps = make_params(p, x, x, x, a, b, z, A_log, dt_bias, norm_w, state_pool, cu_seqlens, out,
+                                      dims, scale, eps, status_word);
+    if (ps != GDN_OK) return ps;
+    if (!aligned(state_indices, 4) || !aligned(num_accepted, 4) || (spec_token_indx && !aligned(spec_token_indx, 4)) ||
+        !aligned(conv_pool, 8) || (conv_bias && !aligned(conv_bias, 8)) || !aligned(conv_weight, 2) ||
+        !aligned(conv_in, 4) || !aligned(conv_out, 4) || cdims->x_stride % 4 != 0)
+        return GDN_ERR_MISALIGNED;
+    p.idx = state_indices;
+    p.num_acc = num_accepted;
+    p.sti = spec_token_indx;
+    p.conv_dim = 2 * dims->H_k * kK + dims->H_v * kV;
+    p.x = static_cast<const __nv_bfloat16*>(x);
+    p.x_stride = cdims->x_stride ? cdims->x_stride : p.conv_dim;
+    p.conv_w = static_cast<const __nv_bfloat16*>(conv_weight);
+    p.conv_b = static_cast<const __nv_bfloat16*>(conv_bias);
+    p.conv_pool = static_cast<__nv_bfloat16*>(conv_pool);
+    p.conv_in = conv_in;
+    p.conv_out = conv_out;
+    p.num_conv_slots = cdims->num_conv_slots;
+    p.conv_width = cdims->width;
+    p.conv_state_len = cdims->state_len;
+    const int64_t units = static_cast<int64_t>(dims->batch) * dims->H_v;
+    const cudaError_t err =
+        by_state_dtype<ConvDecodeLauncher>(state_dtype, p, units, reinterpret_cast<cudaStream_t>(stream));
     return err == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 

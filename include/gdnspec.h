@@ -226,6 +226,69 @@ GDNSPEC_API gdn_status gdn_prefill_chunked(
     const gdn_dims* dims, float scale, float eps, gdn_dtype state_dtype,
     int32_t* status_word, gdn_stream_t stream);
 
+/* Sizes of the short causal convolution in front of the step (gdn_spec_decode_conv). */
+typedef struct {
+    int32_t width;          /* taps W, 1..4 */
+    int32_t state_len;      /* rows per conv slot; >= W - 1 + spec_stride */
+    int64_t num_conv_slots; /* slots in conv_pool */
+    int64_t x_stride;       /* elements between rows of x; 0 = conv_dim (dense); multiple of 4 */
+    int32_t reserved[2];    /* must be 0 */
+} gdn_conv_dims;
+
+/*
+ * gdn_spec_decode_conv -- gdn_spec_decode with the depthwise causal
+ * convolution that produces q, k and v fused in front of it ("PR #46090
+ * report", implementation step 2: the speculative conv state is a wide
+ * rolling buffer sliced per token, convolved and written back; "PR #51674
+ * report", implementation step 3: the speculative path runs
+ * causal_conv1d_update with rewind before the post-conv decode kernel).
+ *
+ * Instead of q, k, v the call takes the projection rows x
+ * [num_tokens, conv_dim] (bf16, conv_dim = 2 H_k K + H_v V, channels in the
+ * order q | k | v; row r of token t is gathered like every other input).  For
+ * a processed sequence i (one that gdn_spec_decode would not skip), with
+ * a = max(num_accepted[i], 1):
+ *   history   the W-1 rows a .. a+W-2 of conv slot conv_in[i] (zeros when
+ *             conv_in[i] < 0): the inputs up to the previous step's last
+ *             accepted token;
+ *   conv      y_t[c] = silu(bias[c] + sum_{w<W} weight[c][w] x_{t-W+1+w}[c])
+ *             over (history, this step's rows) in time order, in FP32; y
+ *             feeds the step as q | k | v (never rounded to bf16);
+ *   new slot  conv slot conv_out[i] (skipped when < 0): rows 0 .. W-2 = the
+ *             history, rows W-1 .. W-2+q_len = this step's rows, bit for bit;
+ *             later rows are left as they were.
+ * After a prefill the caller seeds a slot with the prompt's last W inputs in
+ * rows 0 .. W-1 and passes num_accepted = 1.
+ *
+ *   x             bf16 [num_tokens, conv_dim], row stride cdims->x_stride
+ *   conv_weight   bf16 [conv_dim, W]
+ *   conv_bias     bf16 [conv_dim], or NULL (no bias)
+ *   conv_pool     bf16 [num_conv_slots, state_len, conv_dim], caller-owned
+ *   conv_in, conv_out  int32 [batch] (device)
+ *   every other argument as for gdn_spec_decode; dims->q_stride, k_stride and
+ *   v_stride are not used, dims->split must be 0 or 1.
+ *
+ * Caller contract (in addition to gdn_spec_decode's): no conv_out[j] >= 0
+ * equals any conv_in[i] of the call (a slot is never read and written by one
+ * step: the CTAs of a sequence share its q / k channels), and the
+ * non-negative conv_out are distinct.  A conv slot >= num_conv_slots sets
+ * GDN_FLAG_SLOT_RANGE and skips the sequence.  Host errors: width outside
+ * 1..4, state_len too small or non-zero reserved -> GDN_ERR_BAD_SHAPE; x /
+ * conv_pool / conv_bias not 8-byte aligned, or x_stride not a multiple of 4
+ * -> GDN_ERR_MISALIGNED.  Asynchronous on `stream`, allocates nothing.
+ */
+GDNSPEC_API gdn_status gdn_spec_decode_conv(
+    const void* x, const void* conv_weight, const void* conv_bias, void* conv_pool,
+    const int32_t* conv_in, const int32_t* conv_out, const gdn_conv_dims* cdims,
+    const void* a, const void* b, const void* z,
+    const float* A_log, const void* dt_bias, const void* norm_w,
+    void* state_pool,
+    const int32_t* state_indices, const int32_t* num_accepted,
+    const int32_t* cu_seqlens, const int32_t* spec_token_indx,
+    void* out,
+    const gdn_dims* dims, float scale, float eps, gdn_dtype state_dtype,
+    int32_t* status_word, gdn_stream_t stream);
+
 /*
  * The CTAs per (sequence, v-head) that gdn_spec_decode would use for these
  * sizes when dims->split == 0 (1, 2, 4 or 8), or 0 for invalid dims.  Host

@@ -58,22 +58,24 @@ def test_version_and_status_strings(lib):
     assert gdn.status_str(99) == "unknown status"
 
 
-def test_dims_struct_layout_matches_c(tmp_path):
+@pytest.mark.parametrize("struct", ["gdn_dims", "gdn_conv_dims"])
+def test_dims_struct_layout_matches_c(tmp_path, struct):
     """Compile a probe against the header and compare sizeof / offsetof with
     the ctypes mirror."""
-    fields = [f for f, _ in binding.gdn_dims._fields_]
+    mirror = getattr(binding, struct)
+    fields = [f for f, _ in mirror._fields_]
     src = tmp_path / "probe.c"
     src.write_text(
         '#include <stdio.h>\n#include <stddef.h>\n#include "gdnspec.h"\nint main(void){\n'
-        '  printf("%zu\\n", sizeof(gdn_dims));\n'
-        + "".join(f'  printf("%zu\\n", offsetof(gdn_dims, {f}));\n' for f in fields)
+        f'  printf("%zu\\n", sizeof({struct}));\n'
+        + "".join(f'  printf("%zu\\n", offsetof({struct}, {f}));\n' for f in fields)
         + "  return 0;\n}\n")
     exe = tmp_path / "probe"
     subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
     vals = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()]
-    assert vals[0] == ctypes.sizeof(binding.gdn_dims)
+    assert vals[0] == ctypes.sizeof(mirror)
     for f, off in zip(fields, vals[1:]):
-        assert getattr(binding.gdn_dims, f).offset == off, f
+        assert getattr(mirror, f).offset == off, f
 
 
 def _dims(**over):
@@ -118,3 +120,37 @@ def test_explicit_split_is_reported(lib):
     for s in (1, 2, 4, 8):
         assert binding.chosen_split(_dims(split=s)) == s
     assert binding.chosen_split(_dims(K=64)) == 0
+
+
+def _cdims(**over):
+    c = binding.gdn_conv_dims()
+    c.width, c.state_len, c.num_conv_slots, c.x_stride = 4, 5, 4, 0
+    for k, v in over.items():
+        if k == "reserved":
+            c.reserved[0] = v
+        else:
+            setattr(c, k, v)
+    return c
+
+
+def _call_conv(lib, dims, cdims, *, ptr=0x1000, bias=0x1000, state_dtype=0):
+    P = ptr
+    return lib.gdn_spec_decode_conv(P, P, bias, P, P, P, ctypes.byref(cdims), P, P, P, P, P, P, P, P, P, P, None, P,
+                                    ctypes.byref(dims), 0.088, 1e-5, state_dtype, None, None)
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(width=0), 2), (dict(width=5), 2), (dict(state_len=4), 2), (dict(num_conv_slots=0), 2),
+    (dict(x_stride=-4), 2), (dict(reserved=1), 2), (dict(x_stride=1026), 4),
+])
+def test_conv_bad_dims_rejected(lib, over, code):
+    assert _call_conv(lib, _dims(), _cdims(**over)) == code
+
+
+def test_conv_bad_pointers_rejected(lib):
+    assert _call_conv(lib, _dims(), _cdims(), ptr=0) == 1        # NULL tensors
+    assert _call_conv(lib, _dims(), _cdims(), bias=0x1002) == 4   # bias not 8-byte aligned
+    assert _call_conv(lib, _dims(split=2), _cdims()) == 3         # the fused path has no split
+    assert _call_conv(lib, _dims(batch=0), _cdims(), ptr=0) == 0  # empty batch: nothing launched
+    assert lib.gdn_spec_decode_conv(*([None] * 6), None, *([None] * 12), ctypes.byref(_dims()), 0.1, 1e-5, 0,
+                                    None, None) == 1
