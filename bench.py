@@ -56,6 +56,10 @@ for _bs, _L in ((4, 1024), (32, 256)):
     WORKLOADS[f"prefill_bs{_bs}_l{_L}_bf16"] = (
         f"prefill: {_bs} prompts x {_L} tokens, H_k=2, H_v=16, K=V=128, bf16 state read from and written to a slot",
         dict(prefill=True, bs=_bs, L=_L))
+WORKLOADS["bs32_t8_bf16_conv"] = (
+    "BS=32, H_k=2, H_v=16, K=V=128, T=8, bf16 state, acceptance U{0..8}, 4096-slot pool, with the width-4 "
+    "causal convolution and its rewind fused in front (bf16 conv slots, 2 per sequence per set)",
+    dict(bs=32, sd="bf16", conv=True))
 WORKLOADS["large_bs256_t8_bf16"] = (
     "BS=256, H_k=4, H_v=32, K=V=128, T=8, bf16 state, acceptance Binomial(8,0.7), 16384-slot (16 GiB) pool",
     dict(large=True))
@@ -474,6 +478,100 @@ def run_ours(args, rank, world, local_rank):
     print(json.dumps(line), flush=True)
 
 
+def run_conv(args, rank, world, local_rank):
+    """The fused-conv workload: one step = one gdn_spec_decode_conv call over
+    the batch; N_SETS disjoint sets of state-slot tables, conv slot pairs and
+    projection rows rotate so that no set is read back from L2."""
+    import torch
+
+    import gated_deltanet_linear_sm_gb300 as gdn
+    from gated_deltanet_linear_sm_gb300 import synth
+
+    gdn.load_library()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    case = make_case(args.workload, seed=rank_seed(rank))
+    B = case.batch
+    sets = synth.disjoint_index_sets(case, N_SETS)
+    ci = synth.conv_inputs(case, width=4, num_conv_slots=2 * N_SETS * B, seed=rank_seed(rank))
+
+    def bf(x):
+        return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    tdt = {synth.F32: torch.float32, synth.BF16: torch.bfloat16, synth.F16: torch.float16}[case.state_dtype]
+    g = torch.Generator(device=dev)
+    g.manual_seed(1000 + rank)
+    pool = torch.randn((case.num_slots, case.H_v, case.K, case.V), generator=g, device=dev).mul_(0.1).to(tdt)
+    conv_pool = bf(ci.pool)
+    common = dict(A_log=torch.from_numpy(case.A_log).to(dev), dt_bias=bf(case.dt_bias), norm_w=bf(case.norm_w),
+                  w=bf(ci.weight), bias=bf(ci.bias), acc=torch.from_numpy(case.num_accepted).to(dev),
+                  cu=torch.from_numpy(case.cu_seqlens).to(dev))
+    perm = np.random.default_rng(rank).permutation(ci.pool.shape[0]).astype(np.int32)
+    per_set = []
+    for s in range(N_SETS):
+        rng = np.random.default_rng([rank, s, 9])
+        x = synth.f32_to_bf16_bits(rng.normal(0, 1, ci.x.shape).astype(np.float32)) if s else ci.x
+        per_set.append(dict(
+            x=bf(x), a=bf(case.a), b=bf(case.b), z=bf(case.z), idx=torch.from_numpy(sets[s]).to(dev),
+            cin=torch.from_numpy(perm[2 * s * B:(2 * s + 1) * B].copy()).to(dev),
+            cout=torch.from_numpy(perm[(2 * s + 1) * B:(2 * s + 2) * B].copy()).to(dev)))
+    out = torch.zeros((case.num_tokens, case.H_v, case.V), dtype=torch.bfloat16, device=dev)
+
+    def step(s, stream=None):
+        d = per_set[s % N_SETS]
+        gdn.gdn_spec_decode_conv(d["x"], common["w"], common["bias"], conv_pool, d["cin"], d["cout"], d["a"], d["b"],
+                                 d["z"], common["A_log"], common["dt_bias"], common["norm_w"], pool, d["idx"],
+                                 common["acc"], common["cu"], out, H_k=case.H_k, max_T=8, stream=stream)
+
+    stream = torch.cuda.current_stream(dev)
+    for s in range(max(args.warmup, 3)):
+        step(s)
+    torch.cuda.synchronize()
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except AttributeError:
+        gpu_id = str(local_rank)
+    sampler = ClockSampler(gpu_id)
+    sampler.start()
+    t_soak, n = time.time(), 0
+    while time.time() - t_soak < 0.4:                          # load clocks before the timed region
+        step(n)
+        n += 1
+        if n % 64 == 0:
+            torch.cuda.synchronize()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler.mark("start")
+    e0.record(stream)
+    for s in range(args.steps):
+        step(s, stream.cuda_stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    sampler.mark("end")
+    time.sleep(0.12)
+    sampler.stop()
+    clocks = sampler.summary()
+    ms = max_over_ranks(e0.elapsed_time(e1), world, dev) / args.steps
+    if rank != 0:
+        return
+    updates = synth.token_head_updates(case)
+    alg = synth.conv_algorithmic_bytes(case, ci)
+    peak, peak_kind = measured_peak_gbs()
+    achieved = alg / (ms * 1e-3) / 1e9
+    print(json.dumps({
+        "metric": "token·head updates/s (fused conv + decode)", "value": updates * world / (ms * 1e-3),
+        "unit": "token·head updates/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "us_per_step": ms * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": f"{args.workload}: {WORKLOADS[args.workload][0]}", "global_batch": B * world,
+                   "seq_len": 8, "parallelism": f"independent batches, {world} GPU(s)",
+                   "l2": f"{N_SETS} rotating input / slot sets"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": None, "peak_kind": f"{peak_kind} HBM copy bandwidth",
+                     "algorithmic_bytes_per_launch": alg},
+        "gpu_launches": args.steps, "clocks": clocks}), flush=True)
+
+
 def run_prefill(args, rank, world, local_rank):
     """Prefill workloads: one step = one gdn_prefill call over the batch of
     prompts; each prompt starts from a slot and stores its final state in
@@ -568,6 +666,8 @@ def main():
     try:
         if WORKLOADS[args.workload][1].get("prefill"):
             run_prefill(args, rank, world, local_rank)
+        elif WORKLOADS[args.workload][1].get("conv"):
+            run_conv(args, rank, world, local_rank)
         else:
             run_ours(args, rank, world, local_rank)
     finally:

@@ -403,42 +403,64 @@ __device__ __forceinline__ int conv_row(const Params& p, int bos, int tau) {
 
 // q, k, v of draft token t for this lane's channels: y = silu(bias + sum_w
 // weight[w] x_{t-W+1+w}) over (the W-1 history rows at `hist`, null for zero
-// history; then the step's rows), FP32.  Sets `bad` for an out-of-range row.
+// history; then the step's rows), FP32.  Every load of the token is issued
+// before the arithmetic.  Sets `bad` for an out-of-range row.
 __device__ __forceinline__ void conv_token(const Params& p, int bos, int t, const int (&ch)[3],
                                            const __nv_bfloat16* hist, float (&y)[3][4], int& bad) {
     const int W = p.conv_width;
+    uint2 raw[4][3];
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+        const int tau = t - (W - 1) + w;
+        const __nv_bfloat16* src = nullptr;
+        if (w < W) {
+            if (tau < 0) {
+                if (hist != nullptr) src = hist + static_cast<int64_t>(W - 1 + tau) * p.conv_dim;
+            } else {
+                const int r = conv_row(p, bos, tau);
+                if (r < 0) bad = 1;
+                else src = p.x + r * p.x_stride;
+            }
+        }
+#pragma unroll
+        for (int g = 0; g < 3; ++g) raw[w][g] = src != nullptr ? ldg_quad(src + ch[g]) : make_uint2(0, 0);
+    }
+    // per group: bias, weights ([channel][W]: one 32-byte run per 4 channels
+    // when W = 4; these stay in L1 across tokens), then the taps
 #pragma unroll
     for (int g = 0; g < 3; ++g) {
+        float wt[4][4];
+        if (W == 4) {
+            const uint4* wp = reinterpret_cast<const uint4*>(p.conv_w + static_cast<int64_t>(ch[g]) * 4);
+            const uint4 w0 = __ldg(wp), w1 = __ldg(wp + 1);
+            const uint32_t ww[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ww[j]));
+                wt[j >> 1][(2 * j) & 3] = f.x;
+                wt[j >> 1][(2 * j + 1) & 3] = f.y;
+            }
+        } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+#pragma unroll
+                for (int w = 0; w < 4; ++w)
+                    wt[e][w] = w < W ? __bfloat162float(p.conv_w[static_cast<int64_t>(ch[g] + e) * W + w]) : 0.f;
+        }
         float b4[4] = {0.f, 0.f, 0.f, 0.f};
         if (p.conv_b != nullptr) unpack_bf16x4(ldg_quad(p.conv_b + ch[g]), b4);
 #pragma unroll
         for (int e = 0; e < 4; ++e) y[g][e] = b4[e];
-    }
 #pragma unroll
-    for (int w = 0; w < 4; ++w) {
-        if (w >= W) break;
-        const int tau = t - (W - 1) + w;
-        const __nv_bfloat16* src = nullptr;
-        if (tau < 0) {
-            if (hist != nullptr) src = hist + static_cast<int64_t>(W - 1 + tau) * p.conv_dim;
-        } else {
-            const int r = conv_row(p, bos, tau);
-            if (r < 0) bad = 1;
-            else src = p.x + r * p.x_stride;
+        for (int w = 0; w < 4; ++w) {
+            float u[4];
+            unpack_bf16x4(raw[w][g], u);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) y[g][e] = fmaf(wt[e][w], u[e], y[g][e]);
         }
 #pragma unroll
-        for (int g = 0; g < 3; ++g) {
-            float u[4] = {0.f, 0.f, 0.f, 0.f};
-            if (src != nullptr) unpack_bf16x4(ldg_quad(src + ch[g]), u);
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-                y[g][e] = fmaf(__bfloat162float(p.conv_w[static_cast<int64_t>(ch[g] + e) * W + w]), u[e], y[g][e]);
-        }
+        for (int e = 0; e < 4; ++e) y[g][e] = __fdividef(y[g][e], 1.0f + __expf(-y[g][e]));   // SiLU
     }
-#pragma unroll
-    for (int g = 0; g < 3; ++g)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) y[g][e] = y[g][e] / (1.0f + expf(-y[g][e]));
 }
 
 // ---- the speculative decode kernel -------------------------------------------------
@@ -872,7 +894,8 @@ gdn_status gdn_spec_decode_conv(const void* x, const void* conv_weight, const vo
                                       dims, scale, eps, status_word);
     if (ps != GDN_OK) return ps;
     if (!aligned(state_indices, 4) || !aligned(num_accepted, 4) || (spec_token_indx && !aligned(spec_token_indx, 4)) ||
-        !aligned(conv_pool, 8) || (conv_bias && !aligned(conv_bias, 8)) || !aligned(conv_weight, 2) ||
+        !aligned(conv_pool, 8) || (conv_bias && !aligned(conv_bias, 8)) ||
+        !aligned(conv_weight, cdims->width == 4 ? 16 : 2) ||
         !aligned(conv_in, 4) || !aligned(conv_out, 4) || cdims->x_stride % 4 != 0)
         return GDN_ERR_MISALIGNED;
     p.idx = state_indices;

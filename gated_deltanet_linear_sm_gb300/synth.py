@@ -434,3 +434,23 @@ def conv_inputs(case: Case, width: int = 4, num_conv_slots: int | None = None, w
     perm = rng.permutation(ns).astype(np.int32)
     return ConvInputs(width=width, state_len=state_len, x=x, weight=weight, bias=bias, pool=pool,
                       conv_in=perm[:case.batch].copy(), conv_out=perm[case.batch:2 * case.batch].copy())
+
+
+def conv_algorithmic_bytes(case: Case, ci: ConvInputs, out_bytes: int = 2) -> int:
+    """algorithmic_bytes of the step (x rows hold the same channels as q, k, v)
+    plus, per processed sequence, the W-1 history rows read, the W-1+q_len
+    rows of the new conv slot written, and the conv weights, bias and slot
+    indices once."""
+    D, W = ci.conv_dim, ci.width
+    ql = case.q_lens()
+    rs = case.read_slots()
+    conv = 0
+    for i in range(case.batch):
+        if ql[i] <= 0 or rs[i] < 0 or rs[i] >= case.num_slots:
+            continue
+        if ci.conv_in[i] >= 0:
+            conv += (W - 1) * D * 2
+        if ci.conv_out[i] >= 0:
+            conv += (W - 1 + int(ql[i])) * D * 2
+    conv += D * W * 2 + (D * 2 if ci.bias is not None else 0) + 8 * case.batch
+    return algorithmic_bytes(case, out_bytes) + conv

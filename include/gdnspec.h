@@ -274,8 +274,8 @@ typedef struct {
  * non-negative conv_out are distinct.  A conv slot >= num_conv_slots sets
  * GDN_FLAG_SLOT_RANGE and skips the sequence.  Host errors: width outside
  * 1..4, state_len too small or non-zero reserved -> GDN_ERR_BAD_SHAPE; x /
- * conv_pool / conv_bias not 8-byte aligned, or x_stride not a multiple of 4
- * -> GDN_ERR_MISALIGNED.  Asynchronous on `stream`, allocates nothing.
+ * conv_pool / conv_bias not 8-byte aligned, conv_weight not 16-byte aligned
+ * when W = 4, or x_stride not a multiple of 4 -> GDN_ERR_MISALIGNED.  Asynchronous on `stream`, allocates nothing.
  */
 GDNSPEC_API gdn_status gdn_spec_decode_conv(
     const void* x, const void* conv_weight, const void* conv_bias, void* conv_pool,
