@@ -163,21 +163,29 @@ def measured_peak_gbs():
         return 6800.0, "fallback"
 
 
+KERNEL_SOURCES = ("gated_deltanet_linear_sm_gb300/csrc/gdnspec.cu",
+                  "gated_deltanet_linear_sm_gb300/csrc/gdnprefill_chunked.cu",
+                  "gated_deltanet_linear_sm_gb300/csrc/gdn_internal.h")
+
+
 def kernel_source_hash():
+    """First 16 hex digits of the SHA-256 of the kernel sources."""
     h = hashlib.sha256()
-    for p in ("gated_deltanet_linear_sm_gb300/csrc/gdnspec.cu", "include/gdnspec.h"):
+    for p in KERNEL_SOURCES:
         with open(os.path.join(ROOT, p), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
 def profiled_traffic(workload):
-    """DRAM bytes per launch from the committed ncu summary for this workload,
-    if it was taken on the current kernel source; else None."""
-    path = os.path.join(ROOT, "profiles", f"gdn_spec_decode_kernel_{workload}.md")
+    """DRAM bytes per launch from the committed ncu summary for this workload
+    (profiles/<kernel>_<workload>.md), if it was taken on the current kernel
+    sources; else None."""
+    import glob
+    paths = sorted(glob.glob(os.path.join(ROOT, "profiles", f"*_{workload}.md")))
     try:
-        text = open(path).read()
-    except OSError:
+        text = open(paths[0]).read()
+    except (OSError, IndexError):
         return None
     m = re.search(r"traffic_bytes_per_launch:\s*(\d+)", text)
     s = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
@@ -567,7 +575,7 @@ def run_conv(args, rank, world, local_rank):
                    "seq_len": 8, "parallelism": f"independent batches, {world} GPU(s)",
                    "l2": f"{N_SETS} rotating input / slot sets"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": None, "peak_kind": f"{peak_kind} HBM copy bandwidth",
+                     "traffic": profiled_traffic(args.workload), "peak_kind": f"{peak_kind} HBM copy bandwidth",
                      "algorithmic_bytes_per_launch": alg},
         "gpu_launches": args.steps, "clocks": clocks}), flush=True)
 
@@ -635,8 +643,8 @@ def run_prefill(args, rank, world, local_rank):
                    "global_batch": B * world,
                    "seq_len": int(case.q_lens().max()), "parallelism": f"independent batches, {world} GPU(s)"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": None, "peak_kind": f"{peak_kind} HBM copy bandwidth",
-                     "algorithmic_bytes_per_launch": alg},
+                     "traffic": profiled_traffic(args.workload) if args.prefill_form == "chunked" else None,
+                     "peak_kind": f"{peak_kind} HBM copy bandwidth", "algorithmic_bytes_per_launch": alg},
         "gpu_launches": args.steps}), flush=True)
 
 
