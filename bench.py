@@ -417,24 +417,54 @@ def run_ours(args, rank, world, local_rank):
 
     # --- end to end through the public API with host buffers ---
     # every step: one pinned host-to-device copy of the step's inputs, the
-    # call, and a device-to-host read of its output
+    # call, and a device-to-host read of its output.  Copies run on their own
+    # streams, so step s+1's inputs travel while step s computes and step s's
+    # output travels back while step s+1 computes; events keep each of the
+    # N_SETS buffer sets free until the step that last used it has finished.
     h2d = total
     d2h = host_bufs[0][1].numel() * host_bufs[0][1].element_size()
+    up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev = lambda: torch.cuda.Event()
+    h2d_done = [ev() for _ in range(N_SETS)]
+    run_done = [ev() for _ in range(N_SETS)]
+    d2h_done = [ev() for _ in range(N_SETS)]
+    used = [False] * N_SETS
 
     def e2e_step(s):
-        (hb, hout), t = host_bufs[s % N_SETS], inputs[s % N_SETS]
-        t["buf"].copy_(hb, non_blocking=True)
-        calls[s % N_SETS](stream.cuda_stream)
-        hout.copy_(t["out"], non_blocking=True)
+        k = s % N_SETS
+        (hb, hout), t = host_bufs[k], inputs[k]
+        if used[k]:
+            up.wait_event(run_done[k])                 # the set's inputs were consumed
+        with torch.cuda.stream(up):
+            t["buf"].copy_(hb, non_blocking=True)
+        h2d_done[k].record(up)
+        stream.wait_event(h2d_done[k])
+        if used[k]:
+            stream.wait_event(d2h_done[k])             # the set's previous output was read back
+        calls[k](stream.cuda_stream)
+        run_done[k].record(stream)
+        down.wait_event(run_done[k])
+        with torch.cuda.stream(down):
+            hout.copy_(t["out"], non_blocking=True)
+        d2h_done[k].record(down)
+        used[k] = True
+
+    def e2e_drain():
+        for k in range(N_SETS):
+            if used[k]:
+                stream.wait_event(d2h_done[k])
 
     for s in range(3):
         e2e_step(s)
+    e2e_drain()
     torch.cuda.synchronize()
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
+    up.wait_event(e0)
     for s in range(args.steps):
         e2e_step(s)
+    e2e_drain()
     e1.record(stream)
     torch.cuda.synchronize()
     barrier()
