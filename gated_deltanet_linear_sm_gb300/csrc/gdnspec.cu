@@ -1,7 +1,10 @@
 // libgdnspec: the Gated DeltaNet speculative / MTP decode step for sm_103a.
 //
-// What one call computes is stated in include/gdnspec.h, with the report
-// pages it follows.  This file holds the kernel and the C-ABI host code.
+// What each call computes is stated in include/gdnspec.h, with the report
+// pages it follows.  This file holds the decode kernel (and its variant with
+// the short causal convolution fused in front), the per-token prefill kernel,
+// and every C entry point with its host-side checks; the tensor-core chunked
+// prefill kernel is in gdnprefill_chunked.cu.
 //
 // Design (GB300):
 //  * The step is HBM-bound: one 128x128 state tile read and up to 8 tile writes
@@ -32,6 +35,14 @@
 //    mean-square over V is then combined through distributed shared memory.
 //  * No device-side waits on flags, no traps: bad device data is skipped and
 //    reported through an optional status word.
+//  * Fused convolution (CONV = true, SPLIT = 1): each lane convolves its 12
+//    channels (4 of q, 4 of k, 4 of v) for its warp's draft token from the
+//    rewound history rows and the step's rows, all loads first, in FP32; the
+//    result enters the same per-token prologue.  The new conv slot is written
+//    once the sequence is known not to be skipped.
+//  * Prefill (per token): the same token step over whole prompts, 8 tokens
+//    per round of prologue / tokens / epilogue, the state in registers from
+//    the first token to the last and stored once.
 
 #include <cooperative_groups.h>
 #include <cuda_bf16.h>
@@ -164,6 +175,26 @@ __device__ __forceinline__ void raise_flag(const Params& p, int rank, int flag) 
     if (p.status != nullptr && threadIdx.x == 0 && rank == 0) atomicOr(p.status, flag);
 }
 
+// Paired FP32 arithmetic (fma.rn.f32x2 / mul.rn.f32x2): each lane of the pair
+// rounds exactly as fmaf / a plain multiply would, at half the instructions.
+__device__ __forceinline__ uint64_t pk2(float a, float b) {
+    return (static_cast<uint64_t>(__float_as_uint(b)) << 32) | __float_as_uint(a);
+}
+__device__ __forceinline__ void upk2(uint64_t v, float& a, float& b) {
+    a = __uint_as_float(static_cast<uint32_t>(v));
+    b = __uint_as_float(static_cast<uint32_t>(v >> 32));
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
 // ---- the pieces of one unit ------------------------------------------------------
 
 // Per-token prologue arithmetic for token t of unit (i, h), one warp: the raw
@@ -241,9 +272,13 @@ __device__ __forceinline__ void token_step(float (&S)[kRowsPerLane][4], Smem& s,
 #pragma unroll
         for (int rr = 0; rr < 4; ++rr)
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                x[c] = fmaf(S[4 * r4 + rr][c], kr[rr], x[c]);
-                x[4 + c] = fmaf(S[4 * r4 + rr][c], qr[rr], x[4 + c]);
+            for (int c = 0; c < 4; c += 2) {                   // column pairs
+                const uint64_t s2 = pk2(S[4 * r4 + rr][c], S[4 * r4 + rr][c + 1]);
+                uint64_t xk = pk2(x[c], x[c + 1]), xq = pk2(x[4 + c], x[5 + c]);
+                xk = ffma2(s2, pk2(kr[rr], kr[rr]), xk);
+                xq = ffma2(s2, pk2(qr[rr], qr[rr]), xq);
+                upk2(xk, x[c], x[c + 1]);
+                upk2(xq, x[4 + c], x[5 + c]);
             }
     }
     // reduce-scatter over the 8 row groups (lane bits 4, 3, 2): afterwards
@@ -291,8 +326,11 @@ __device__ __forceinline__ void token_step(float (&S)[kRowsPerLane][4], Smem& s,
 #pragma unroll
         for (int rr = 0; rr < 4; ++rr)
 #pragma unroll
-            for (int c = 0; c < 4; ++c)
-                S[4 * r4 + rr][c] = fmaf(S[4 * r4 + rr][c], decay, kr[rr] * vpc[c]);
+            for (int c = 0; c < 4; c += 2) {                   // S = fmaf(S, decay, k v'), by pairs
+                const uint64_t t2 = fmul2(pk2(kr[rr], kr[rr]), pk2(vpc[c], vpc[c + 1]));
+                const uint64_t s2 = ffma2(pk2(S[4 * r4 + rr][c], S[4 * r4 + rr][c + 1]), pk2(decay, decay), t2);
+                upk2(s2, S[4 * r4 + rr][c], S[4 * r4 + rr][c + 1]);
+            }
     }
 
     // the state after token t goes to slot s.ws[t] (skip -1)
