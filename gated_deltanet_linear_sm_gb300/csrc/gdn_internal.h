@@ -5,6 +5,7 @@
 // include/gdnspec.h.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -16,6 +17,7 @@ namespace gdn_internal {
 
 // Filled on the host from one validated call; passed by value to the kernels.
 struct Params {
+    CUtensorMap pool_map;            // decode: the state pool as [slots * H_v * K rows][V], box 128 x 16
     const __nv_bfloat16* q;
     const __nv_bfloat16* k;
     const __nv_bfloat16* v;

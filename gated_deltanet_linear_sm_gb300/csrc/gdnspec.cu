@@ -51,6 +51,8 @@
 
 #include <cstdint>
 
+#include <cudaTypedefs.h>
+
 #include "gdn_internal.h"
 #include "gdnspec.h"
 
@@ -72,6 +74,10 @@ constexpr int64_t kTile = static_cast<int64_t>(kK) * kV;
 // banks when each reads its 16-byte chunk
 constexpr int kKPad = kK + kK / 4;
 __host__ __device__ constexpr int kpos(int row) { return row + (row >> 4) * 4; }
+// A lane of row group rg (0..7) holds K rows rg + 8 j, j = 0..15.  k^ / q^ are
+// stored permuted so that those 16 rows are contiguous: row -> 16 (row % 8) +
+// row / 8, then padded as above.
+__host__ __device__ constexpr int kperm(int row) { return kpos((row & 7) * 16 + (row >> 3)); }
 
 using gdn_internal::Params;
 
@@ -92,7 +98,11 @@ template <typename StateT, int SPLIT>
 struct Config {
     static constexpr int kWarps = 8 / SPLIT;
     static constexpr int kThreads = 32 * kWarps;
-    static constexpr size_t kSmem = sizeof(Smem);
+    // each warp stages its 128 x 16 block of a token's state for the tensor store
+    static constexpr size_t kStageOffset = (sizeof(Smem) + 127) / 128 * 128;
+    static constexpr size_t kStageElems = static_cast<size_t>(kK) * kColsPerWarp;
+    // + 128 bytes so that the staging buffers can start on a 128-byte boundary
+    static constexpr size_t kSmem = kStageOffset + kWarps * kStageElems * sizeof(StateT) + 128;
 };
 
 // ---- element I/O ---------------------------------------------------------------
@@ -131,6 +141,9 @@ struct StateIO<float> {
     static __device__ __forceinline__ void store4(float* p, const float (&x)[4]) {
         __stcs(reinterpret_cast<float4*>(p), make_float4(x[0], x[1], x[2], x[3]));
     }
+    static __device__ __forceinline__ void stage4(float* p, const float (&x)[4]) {
+        *reinterpret_cast<float4*>(p) = make_float4(x[0], x[1], x[2], x[3]);
+    }
 };
 
 template <>
@@ -141,6 +154,9 @@ struct StateIO<__nv_bfloat16> {
     static __device__ __forceinline__ uint2 pack(const float (&x)[4]) { return pack_bf16x4(x); }
     static __device__ __forceinline__ void store4(__nv_bfloat16* p, const float (&x)[4]) {
         __stcs(reinterpret_cast<uint2*>(p), pack(x));
+    }
+    static __device__ __forceinline__ void stage4(__nv_bfloat16* p, const float (&x)[4]) {
+        *reinterpret_cast<uint2*>(p) = pack(x);
     }
 };
 
@@ -163,7 +179,25 @@ struct StateIO<__half> {
     static __device__ __forceinline__ void store4(__half* p, const float (&x)[4]) {
         __stcs(reinterpret_cast<uint2*>(p), pack(x));
     }
+    static __device__ __forceinline__ void stage4(__half* p, const float (&x)[4]) {
+        *reinterpret_cast<uint2*>(p) = pack(x);
+    }
 };
+
+// ---- tensor (TMA) stores of a warp's staged block ------------------------------------
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+// store the 128 x 16 box at smem `src` to global columns x.., rows y.. of the pool map
+__device__ __forceinline__ void tma_store_box(const CUtensorMap* map, const void* src, int x, int y) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];"
+                 ::"l"(reinterpret_cast<uint64_t>(map)), "r"(smem_addr(src)), "r"(x), "r"(y) : "memory");
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// this thread's earlier tensor stores have finished reading shared memory
+__device__ __forceinline__ void tma_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// ... and have completed
+__device__ __forceinline__ void tma_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll
@@ -221,8 +255,11 @@ __device__ __forceinline__ void prologue_token_f(Smem& s, const Params& p, int h
 #pragma unroll
     for (int e = 0; e < 4; ++e) { qv[e] *= rq; kv[e] *= rk; kq += qv[e] * kv[e]; }
     kq = warp_sum(kq);
-    *reinterpret_cast<float4*>(&s.q[t][kpos(lane * 4)]) = make_float4(qv[0], qv[1], qv[2], qv[3]);
-    *reinterpret_cast<float4*>(&s.k[t][kpos(lane * 4)]) = make_float4(kv[0], kv[1], kv[2], kv[3]);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        s.q[t][kperm(lane * 4 + e)] = qv[e];
+        s.k[t][kperm(lane * 4 + e)] = kv[e];
+    }
     *reinterpret_cast<float4*>(&s.v[t][lane * 4]) = make_float4(vv[0], vv[1], vv[2], vv[3]);
     s.z[t][lane] = zraw;
     if (lane == 0) {
@@ -250,7 +287,7 @@ __device__ __forceinline__ void prologue_token(Smem& s, const Params& p, int h, 
 // slot write.
 template <typename StateT>
 __device__ __forceinline__ void token_step(float (&S)[kRowsPerLane][4], Smem& s, const Params& p, int t, int h,
-                                           int lane, int col0, int row0, int rank) {
+                                           int lane, int col0, int row0, int rank, StateT* stage) {
     const int cgi = lane & 3;
     const int rg = lane >> 2;
     const int c_own = rg & 3;          // after the reduce-scatter: my column ...
@@ -333,13 +370,30 @@ __device__ __forceinline__ void token_step(float (&S)[kRowsPerLane][4], Smem& s,
             }
     }
 
-    // the state after token t goes to slot s.ws[t] (skip -1)
+    // the state after token t goes to slot s.ws[t] (skip -1).  With a staging
+    // buffer the warp writes its 128 x 16 block to shared memory (8 lanes of a
+    // row group fill 8 consecutive 32 / 64-byte rows: no bank conflicts) and
+    // one lane hands it to the tensor-memory-access unit, which writes the
+    // strided block to the slot; the buffer is reused once that store has
+    // read it.  Without one, every lane stores its rows itself.
     const long long ws = s.ws[t];
     if (ws >= p.num_slots) raise_flag(p, rank, GDN_FLAG_SLOT_RANGE);
     if (ws >= 0 && ws < p.num_slots) {
-        StateT* d = static_cast<StateT*>(p.pool) + (ws * p.H_v + h) * kTile + static_cast<int64_t>(row0) * kV + col0;
+        if (stage != nullptr) {
+            if (lane == 0) tma_wait_read();
+            __syncwarp();
 #pragma unroll
-        for (int r = 0; r < kRowsPerLane; ++r) StateIO<StateT>::store4(d + r * kV, S[r]);
+            for (int r = 0; r < kRowsPerLane; ++r)
+                StateIO<StateT>::stage4(stage + (rg + 8 * r) * kColsPerWarp + 4 * cgi, S[r]);
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            if (lane == 0)
+                tma_store_box(&p.pool_map, stage, col0 - 4 * cgi, static_cast<int>((ws * p.H_v + h) * kK));
+        } else {
+            StateT* d = static_cast<StateT*>(p.pool) + (ws * p.H_v + h) * kTile + col0;
+#pragma unroll
+            for (int r = 0; r < kRowsPerLane; ++r) StateIO<StateT>::store4(d + static_cast<int64_t>(rg + 8 * r) * kV, S[r]);
+        }
     }
 }
 
@@ -507,10 +561,10 @@ __device__ __forceinline__ void conv_token(const Params& p, int bos, int t, cons
 // Block: 8 / SPLIT warps, each owning 16 of the unit's 128 V columns.
 template <typename StateT, int SPLIT, bool CONV = false>
 __global__ void __launch_bounds__(Config<StateT, SPLIT>::kThreads, 2 * SPLIT)
-gdn_spec_decode_kernel(const Params p) {
+gdn_spec_decode_kernel(const __grid_constant__ Params p) {
     using C = Config<StateT, SPLIT>;
     constexpr int W = C::kWarps;
-    extern __shared__ __align__(16) unsigned char smem_raw[];
+    extern __shared__ __align__(128) unsigned char smem_raw[];
     Smem& s = *reinterpret_cast<Smem*>(smem_raw);
 
     const int warp = threadIdx.x >> 5;
@@ -557,12 +611,13 @@ gdn_spec_decode_kernel(const Params p) {
         }
     }
 
-    // ---- load this lane's 16x4 block of the state tile (FP32 in registers) ----
+    // ---- load this lane's 16x4 block of the state tile (FP32 in registers):
+    //      rows rg + 8 r, columns col0 .. col0 + 3 ----
     const StateT* src = static_cast<const StateT*>(p.pool) + (rs * p.H_v + h) * kTile;
     float S[kRowsPerLane][4];
 #pragma unroll
     for (int r = 0; r < kRowsPerLane; ++r)
-        StateIO<StateT>::load4(src + static_cast<int64_t>(row0 + r) * kV + col0, S[r]);
+        StateIO<StateT>::load4(src + static_cast<int64_t>(rg + 8 * r) * kV + col0, S[r]);
 
     // ---- per-token prologue: gather rows, gates, normalised q / k, v, z ----
     const int kh = h / p.group;
@@ -633,11 +688,16 @@ gdn_spec_decode_kernel(const Params p) {
     }
 
     // ---- the draft tokens, in order ----
-    for (int t = 0; t < q_len; ++t) token_step<StateT>(S, s, p, t, h, lane, col0, row0, rank);
+    // this warp's staging buffer for the tensor stores (128-byte aligned)
+    StateT* stage = reinterpret_cast<StateT*>(smem_raw + C::kStageOffset +
+                                              ((128u - (smem_addr(smem_raw) & 127u)) & 127u)) +
+                    warp * C::kStageElems;
+    for (int t = 0; t < q_len; ++t) token_step<StateT>(S, s, p, t, h, lane, col0, row0, rank, stage);
 
     // ---- gated RMSNorm epilogue ----
     __syncthreads();                                           // s.o of this CTA complete
     epilogue<SPLIT>(s, p, h, q_len, warp, lane, rank);
+    if (lane == 0) tma_wait_all();                              // the slot writes have landed
 }
 
 // ---- the prefill kernel (recurrent form) -------------------------------------------
@@ -648,7 +708,7 @@ gdn_spec_decode_kernel(const Params p) {
 // last; only the final state is stored.
 template <typename StateT>
 __global__ void __launch_bounds__(256, 2) gdn_prefill_kernel(const Params p) {
-    extern __shared__ __align__(16) unsigned char smem_raw[];
+    extern __shared__ __align__(128) unsigned char smem_raw[];
     Smem& s = *reinterpret_cast<Smem*>(smem_raw);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -673,7 +733,7 @@ __global__ void __launch_bounds__(256, 2) gdn_prefill_kernel(const Params p) {
         const StateT* src = static_cast<const StateT*>(p.pool) + (rs * p.H_v + h) * kTile;
 #pragma unroll
         for (int r = 0; r < kRowsPerLane; ++r)
-            StateIO<StateT>::load4(src + static_cast<int64_t>(row0 + r) * kV + col0, S[r]);
+            StateIO<StateT>::load4(src + static_cast<int64_t>(rg + 8 * r) * kV + col0, S[r]);
     } else {
 #pragma unroll
         for (int r = 0; r < kRowsPerLane; ++r)
@@ -691,15 +751,15 @@ __global__ void __launch_bounds__(256, 2) gdn_prefill_kernel(const Params p) {
             prologue_token(s, p, h, warp, r, lane, qraw, kraw, vraw, zraw, -1);
         }
         __syncthreads();                                       // prologue published
-        for (int t = 0; t < n; ++t) token_step<StateT>(S, s, p, t, h, lane, col0, row0, 0);
+        for (int t = 0; t < n; ++t) token_step<StateT>(S, s, p, t, h, lane, col0, row0, 0, nullptr);
         __syncthreads();                                       // s.o complete
         epilogue<1>(s, p, h, n, warp, lane, 0);
         __syncthreads();                                       // before the next round overwrites s
     }
     if (wsl >= 0) {
-        StateT* d = static_cast<StateT*>(p.pool) + (wsl * p.H_v + h) * kTile + static_cast<int64_t>(row0) * kV + col0;
+        StateT* d = static_cast<StateT*>(p.pool) + (wsl * p.H_v + h) * kTile + col0;
 #pragma unroll
-        for (int r = 0; r < kRowsPerLane; ++r) StateIO<StateT>::store4(d + r * kV, S[r]);
+        for (int r = 0; r < kRowsPerLane; ++r) StateIO<StateT>::store4(d + static_cast<int64_t>(rg + 8 * r) * kV, S[r]);
     }
 }
 
@@ -762,6 +822,57 @@ cudaError_t launch_prefill(const Params& p, int64_t units, cudaStream_t stream) 
 }
 
 bool aligned(const void* ptr, uintptr_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }
+
+// The state pool as a 2-D tensor for the decode kernel's per-warp tensor
+// stores: rows = slots * H_v * K, columns = V, box = 128 rows x 16 columns.
+// cuTensorMapEncodeTiled is reached through the runtime's driver entry point
+// (no link against the driver library); maps are cached per host thread for
+// the last few pools, so a steady stream of calls encodes nothing.
+gdn_status make_pool_map(Params& p, void* pool, int64_t num_slots, int32_t H_v, gdn_dtype dt) {
+    using Encode = PFN_cuTensorMapEncodeTiled_v12000;
+    static const Encode encode = [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            fn = nullptr;
+        return reinterpret_cast<Encode>(fn);
+    }();
+    if (encode == nullptr) return GDN_ERR_CUDA;
+    const int64_t rows = num_slots * H_v * kK;
+    if (rows > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;      // row coordinates are 32-bit
+    struct Entry {
+        const void* pool;
+        int64_t rows;
+        int dt;
+        CUtensorMap map;
+    };
+    thread_local Entry cache[4] = {};
+    thread_local int next = 0;
+    for (const Entry& e : cache)
+        if (e.pool == pool && e.rows == rows && e.dt == dt) {
+            p.pool_map = e.map;
+            return GDN_OK;
+        }
+    const size_t elem = dt == GDN_F32 ? 4 : 2;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kV), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kV * elem)};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kColsPerWarp), static_cast<cuuint32_t>(kK)};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUtensorMapDataType type = dt == GDN_F32    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                     : dt == GDN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                      : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    CUtensorMap map;
+    if (encode(&map, type, 2, pool, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return GDN_ERR_CUDA;
+    cache[next] = Entry{pool, rows, static_cast<int>(dt), map};
+    next = (next + 1) % 4;
+    p.pool_map = map;
+    return GDN_OK;
+}
 
 // One CTA per unit at every batch size measured (4 to 128 sequences of 16
 // v-heads): splitting a unit's columns over a cluster shortens no per-token
@@ -900,6 +1011,8 @@ gdn_status gdn_spec_decode(const void* q, const void* k, const void* v, const vo
     p.idx = state_indices;
     p.num_acc = num_accepted;
     p.sti = spec_token_indx;
+    const gdn_status ms = make_pool_map(p, state_pool, dims->num_slots, dims->H_v, state_dtype);
+    if (ms != GDN_OK) return ms;
     const int64_t units = static_cast<int64_t>(dims->batch) * dims->H_v;
     const int split = dims->split ? dims->split : choose_split(units);
     const cudaError_t err =
@@ -939,6 +1052,8 @@ gdn_status gdn_spec_decode_conv(const void* x, const void* conv_weight, const vo
     p.idx = state_indices;
     p.num_acc = num_accepted;
     p.sti = spec_token_indx;
+    const gdn_status ms = make_pool_map(p, state_pool, dims->num_slots, dims->H_v, state_dtype);
+    if (ms != GDN_OK) return ms;
     p.conv_dim = 2 * dims->H_k * kK + dims->H_v * kV;
     p.x = static_cast<const __nv_bfloat16*>(x);
     p.x_stride = cdims->x_stride ? cdims->x_stride : p.conv_dim;

@@ -145,6 +145,11 @@ typedef struct {
  *
  * Alignment: state_pool 16 bytes; q, k, v, z, out, norm_w 8 bytes with
  * q/k/v/z/out row strides multiples of 4 elements; int32 tables 4 bytes.
+ * Size limit: num_slots * H_v * K < 2^31 (the slot writes address the pool
+ * as one 2-D tensor with 32-bit row coordinates); beyond it the call returns
+ * GDN_ERR_UNSUPPORTED.  The call encodes that tensor's description on the
+ * host the first time it sees a pool (cached per host thread for the last 4
+ * pools); no device memory is allocated.
  */
 GDNSPEC_API gdn_status gdn_spec_decode(
     const void* q, const void* k, const void* v,
