@@ -839,9 +839,9 @@ gdn_status make_pool_map(Params& p, void* pool, int64_t num_slots, int32_t H_v, 
             fn = nullptr;
         return reinterpret_cast<Encode>(fn);
     }();
-    if (encode == nullptr) return GDN_ERR_CUDA;
     const int64_t rows = num_slots * H_v * kK;
     if (rows > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;      // row coordinates are 32-bit
+    if (encode == nullptr) return GDN_ERR_CUDA;
     struct Entry {
         const void* pool;
         int64_t rows;

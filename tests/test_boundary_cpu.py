@@ -154,3 +154,11 @@ def test_conv_bad_pointers_rejected(lib):
     assert _call_conv(lib, _dims(batch=0), _cdims(), ptr=0) == 0  # empty batch: nothing launched
     assert lib.gdn_spec_decode_conv(*([None] * 6), None, *([None] * 12), ctypes.byref(_dims()), 0.1, 1e-5, 0,
                                     None, None) == 1
+
+
+def test_pool_beyond_32bit_rows_is_unsupported(lib):
+    """The slot writes address the pool as one 2-D tensor with 32-bit row
+    coordinates: num_slots * H_v * 128 must stay below 2^31 (checked before
+    anything touches the GPU)."""
+    assert _call(lib, _dims(num_slots=(1 << 31) // (8 * 128))) == 3
+    assert _call_conv(lib, _dims(num_slots=(1 << 31) // (8 * 128)), _cdims()) == 3
