@@ -579,6 +579,15 @@ gdn_spec_decode_kernel(const __grid_constant__ Params p) {
     const int col0 = wg * kColsPerWarp + cgi * 4;
     const int row0 = rg * kRowsPerLane;
 
+    // Launched with programmatic stream serialization: this CTA may become
+    // resident while the previous kernel in the stream is still running.  It
+    // waits here, before its first global access, until that grid has
+    // completed and its writes are visible; and it lets the next kernel's
+    // CTAs be scheduled as soon as every CTA of this grid has started.  Only
+    // the launch latency between back-to-back steps is hidden.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
     // ---- resolve the work item (every thread computes the same answer) ----
     // The sequence's slot row is read in the same round trip as its length and
     // acceptance, so the read slot costs no extra dependent load.
@@ -787,15 +796,17 @@ cudaError_t launch(const Params& p, int64_t units, cudaStream_t stream) {
     cfg.blockDim = dim3(C::kThreads, 1, 1);
     cfg.dynamicSmemBytes = C::kSmem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    cfg.numAttrs = 0;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     if (SPLIT > 1) {
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = SPLIT;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = SPLIT;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        cfg.numAttrs = 2;
     }
     return cudaLaunchKernelEx(&cfg, kernel, p);
 }
