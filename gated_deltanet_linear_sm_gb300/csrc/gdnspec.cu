@@ -11,10 +11,13 @@
 //    per (sequence, v-head), against ~4 FP32 ops per state element per token.
 //    No tensor cores: per token it is a rank-1 update and two K-reductions.
 //  * Work unit = (sequence i, v-head h).  A warp owns 16 full V columns of the
-//    tile (all 128 K rows): lane = cg + 4*rg holds rows 16rg..16rg+15 of columns
-//    16*wg + 4cg .. +3 in 64 registers, FP32, for all draft tokens.  Because
-//    each V column evolves on its own, the two K-reductions are warp-local
-//    shuffles and the token loop needs no block barrier for the math.
+//    tile (all 128 K rows): lane = cg + 4*rg holds rows rg, rg+8, .., rg+120 of
+//    columns 16*wg + 4cg .. +3 in 64 registers, FP32, for all draft tokens.
+//    Because each V column evolves on its own, the two K-reductions are
+//    warp-local shuffles and the token loop needs no block barrier for the
+//    math.  One CTA per unit: the block scheduler starts the next CTA on an
+//    SM as soon as one ends (a grid of resident CTAs walking the units, with
+//    the next unit's tile prefetched into L2, was measured slower).
 //  * Latency: every load that does not depend on another is issued up front.
 //    The tile is read straight into registers with 16-byte (FP32) / 8-byte
 //    (BF16, FP16) streaming loads before the per-token prologue, and the
@@ -24,12 +27,12 @@
 //    the PR #51674 report, implementation step 1): with d = e^g,
 //        u = d (S^T k^),   v' = beta (v - u),   o = d (S^T q^) + (k^.q^) v'
 //    which equals o = S_new^T q^ exactly in real arithmetic.
-//  * Each token's state is stored from registers with streaming vector stores
-//    (each group of 4 lanes covers a contiguous 64 B / 32 B row segment),
-//    rounded once to the pool dtype (RNE) while the carried state stays FP32
-//    (PR #52191 report, implementation step 4).  Staging the tile in shared
-//    memory for full-line stores was measured slower: the per-token CTA
-//    barrier it needs costs more than the partial-line stores.
+//  * Each token's state is rounded once to the pool dtype (RNE) while the
+//    carried state stays FP32 (PR #52191 report, implementation step 4).  Each
+//    warp writes its 128 x 16 block to its own staging buffer in shared memory
+//    and one lane hands it to the tensor-memory-access unit as one 2-D store
+//    into the slot; a warp-level barrier is all it needs (a CTA-wide tile and
+//    barrier per token was measured slower).
 //  * Small batches may split the 8 column blocks of a unit over SPLIT CTAs of
 //    one thread-block cluster (SPLIT = 2, 4, 8); the gated RMSNorm's
 //    mean-square over V is then combined through distributed shared memory.

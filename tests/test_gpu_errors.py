@@ -121,3 +121,32 @@ def test_no_status_word_is_fine():
     torch.cuda.synchronize()
     assert st is None
     compare(case, out, pool, [i for i in range(case.batch) if i != BAD])
+
+
+def test_bad_units_among_many():
+    """1,024 units (64 sequences x 16 v-heads), more than the GPU holds at
+    once, so the CTAs run in several waves.  Sequence BAD has a read slot out
+    of range and sequence 40 a gathered row out of range: both are skipped
+    and flagged, and every other unit, before and after them, still matches
+    the oracle."""
+    case = synth.make_case(batch=64, H_k=2, H_v=16, T=8, state_dtype=synth.BF16, num_slots=1100,
+                           extra_rows=9, seed=35)
+    bad = dataclasses.replace(case, state_indices=case.state_indices.copy(),
+                              spec_token_indx=case.spec_token_indx.copy())
+    j = max(int(case.num_accepted[BAD]) - 1, 0)
+    bad.state_indices[BAD, j] = case.num_slots + 5
+    bad.spec_token_indx[case.cu_seqlens[40] + 1] = case.num_tokens + 3
+    dev = torch.device("cuda", 0)
+    pool = make_pool(case, dev)
+    before = pool.clone()
+    out, pool, st = run_gpu(bad, dev, pool)
+    torch.cuda.synchronize()
+    flags = int(st.item())
+    assert flags & gdn.binding.GDN_FLAG_SLOT_RANGE and flags & gdn.binding.GDN_FLAG_TOKEN_ROW, flags
+    compare(case, out, pool, [i for i in range(case.batch) if i not in (BAD, 40)])
+    for i in (BAD, 40):
+        for s in case.state_indices[i]:
+            if 0 <= s < case.num_slots:
+                assert torch.equal(pool[int(s)].view(torch.int16), before[int(s)].view(torch.int16))
+        rows = torch.from_numpy(_rows_of(case, i).astype(np.int64)).to(dev)
+        assert bool((out.view(torch.int16)[rows] == OUT_SENTINEL).all())
