@@ -247,17 +247,22 @@ __device__ __forceinline__ void prologue_token_f(Smem& s, const Params& p, int h
         dtb = __bfloat162float(p.dt_bias[h]);
         alog = __ldg(p.A_log + h);
     }
-    float sq = 0.f, sk = 0.f;
+    // |q|^2, |k|^2 and q.k in one butterfly: k^.q^ = (q.k) rq rk needs no
+    // second reduction after the normalisation
+    float sq = 0.f, sk = 0.f, qk = 0.f;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) { sq += qv[e] * qv[e]; sk += kv[e] * kv[e]; }
-    sq = warp_sum(sq);
-    sk = warp_sum(sk);
+    for (int e = 0; e < 4; ++e) { sq += qv[e] * qv[e]; sk += kv[e] * kv[e]; qk += qv[e] * kv[e]; }
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) {
+        sq += __shfl_xor_sync(kFull, sq, m);
+        sk += __shfl_xor_sync(kFull, sk, m);
+        qk += __shfl_xor_sync(kFull, qk, m);
+    }
     const float rq = rsqrtf(sq + kQkEps) * p.scale;
     const float rk = rsqrtf(sk + kQkEps);
-    float kq = 0.f;
+    const float kq = qk * rq * rk;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) { qv[e] *= rq; kv[e] *= rk; kq += qv[e] * kv[e]; }
-    kq = warp_sum(kq);
+    for (int e = 0; e < 4; ++e) { qv[e] *= rq; kv[e] *= rk; }
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
         s.q[t][kperm(lane * 4 + e)] = qv[e];
@@ -480,10 +485,9 @@ __device__ __forceinline__ void conv_channels(const Params& p, int kh, int h, in
     ch[2] = 2 * qk + h * kV + lane * 4;
 }
 
-// The W-1 rewound history rows of sequence i in its read slot (rows a ..
-// a+W-2, a = max(num_accepted, 1)), or null for zero history.
-__device__ __forceinline__ const __nv_bfloat16* conv_history(const Params& p, int i, int acc) {
-    const long long ci = __ldg(p.conv_in + i);
+// The W-1 rewound history rows in conv slot ci (rows a .. a+W-2, a =
+// max(num_accepted, 1)), or null for zero history (ci < 0).
+__device__ __forceinline__ const __nv_bfloat16* conv_history(const Params& p, long long ci, int acc) {
     return ci < 0 ? nullptr
                   : p.conv_pool + (ci * p.conv_state_len + max(acc, 1)) * static_cast<int64_t>(p.conv_dim);
 }
@@ -593,7 +597,8 @@ gdn_spec_decode_kernel(const __grid_constant__ Params p) {
 
     // ---- resolve the work item (every thread computes the same answer) ----
     // The sequence's slot row is read in the same round trip as its length and
-    // acceptance, so the read slot costs no extra dependent load.
+    // acceptance, so the read slot costs no extra dependent load; so are the
+    // total token count and, with the convolution, the sequence's conv slots.
     const int32_t* slot_row = p.idx + static_cast<int64_t>(i) * p.stride;
     int slots[kMaxT];
 #pragma unroll
@@ -601,10 +606,16 @@ gdn_spec_decode_kernel(const __grid_constant__ Params p) {
     const int bos = __ldg(p.cu + i);
     const int q_len = __ldg(p.cu + i + 1) - bos;
     const int acc = __ldg(p.num_acc + i);
+    const int cu_total = __ldg(p.cu + p.batch);
+    long long conv_in = -1, conv_out = -1;                     // this sequence's conv slots
+    if constexpr (CONV) {
+        conv_in = __ldg(p.conv_in + i);
+        conv_out = __ldg(p.conv_out + i);
+    }
     if (q_len <= 0) return;                                    // nothing to do
     // token positions must lie inside [0, cu_seqlens[batch]), the length of
     // spec_token_indx (rows themselves are range-checked below)
-    if (bos < 0 || bos + q_len > __ldg(p.cu + p.batch)) { raise_flag(p, rank, GDN_FLAG_TOKEN_ROW); return; }
+    if (bos < 0 || bos + q_len > cu_total) { raise_flag(p, rank, GDN_FLAG_TOKEN_ROW); return; }
     if (acc > p.stride) { raise_flag(p, rank, GDN_FLAG_ACCEPTED); return; }
     if (q_len > p.max_T || q_len > p.stride) { raise_flag(p, rank, GDN_FLAG_QLEN); return; }
     // rewind: the state after the last accepted token; acc-1 clamped at 0
@@ -617,7 +628,7 @@ gdn_spec_decode_kernel(const __grid_constant__ Params p) {
     if (rs < 0) return;                                        // padded sequence
     if (rs >= p.num_slots) { raise_flag(p, rank, GDN_FLAG_SLOT_RANGE); return; }
     if constexpr (CONV) {
-        if (__ldg(p.conv_in + i) >= p.num_conv_slots || __ldg(p.conv_out + i) >= p.num_conv_slots) {
+        if (conv_in >= p.num_conv_slots || conv_out >= p.num_conv_slots) {
             raise_flag(p, rank, GDN_FLAG_SLOT_RANGE);
             return;
         }
@@ -653,7 +664,7 @@ gdn_spec_decode_kernel(const __grid_constant__ Params p) {
                     int conv_ch[3];
                     conv_channels(p, kh, h, lane, conv_ch);
                     float y[3][4];
-                    conv_token(p, bos, t, conv_ch, conv_history(p, i, acc), y, bad);
+                    conv_token(p, bos, t, conv_ch, conv_history(p, conv_in, acc), y, bad);
                     const uint2 zraw = p.z != nullptr
                                            ? ldg_quad(p.z + r * p.z_stride + static_cast<int64_t>(h) * kV + lane * 4)
                                            : make_uint2(0, 0);
@@ -674,11 +685,10 @@ gdn_spec_decode_kernel(const __grid_constant__ Params p) {
     //      v-head h by this unit; q / k channels of the key head by its first
     //      v-head only.  (Only with SPLIT = 1.) ----
     if constexpr (CONV) {
-        const long long conv_out = __ldg(p.conv_out + i);
         if (conv_out >= 0) {
             int conv_ch[3];
             conv_channels(p, kh, h, lane, conv_ch);
-            const __nv_bfloat16* hist = conv_history(p, i, acc);
+            const __nv_bfloat16* hist = conv_history(p, conv_in, acc);
             __nv_bfloat16* dst = p.conv_pool + conv_out * p.conv_state_len * static_cast<int64_t>(p.conv_dim);
             const int g0 = (h % p.group) == 0 ? 0 : 2;
             const int Wc = p.conv_width;
