@@ -394,7 +394,8 @@ def run_ours(args, rank, world, local_rank):
         inputs.append(t)
         host_bufs.append((hb, torch.empty_like(t["out"], device="cpu").pin_memory()))
     calls = [gdn.prepare(t["q"], t["k"], t["v"], t["a"], t["b"], t["z"], t["A_log"], t["dt_bias"], t["norm_w"],
-                         pool, t["state_indices"], t["num_accepted"], t["cu_seqlens"], t["out"], max_T=8)
+                         pool, t["state_indices"], t["num_accepted"], t["cu_seqlens"], t["out"], max_T=8,
+                         split=args.split)
              for t in inputs]
     updates = synth.token_head_updates(case)
     alg_bytes = synth.algorithmic_bytes(case)
@@ -563,7 +564,7 @@ def run_ours(args, rank, world, local_rank):
                          "us_per_step": graph_ms * 1e3 / args.steps},
         "gpu_launches": args.steps,
         "clocks": clocks,
-        "split": gdn.binding.chosen_split(calls[0].dims),
+        "split": gdn.binding.chosen_split(calls[0].dims, calls[0].state_dtype),
     }
     print(json.dumps(line), flush=True)
 
@@ -737,6 +738,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="bs32_t8_bf16")
+    ap.add_argument("--split", type=lambda x: int(x, 0), default=0,
+                    help="decode workloads: dims.split (0 = the library's choice; 1, 2, 4, 8, 0x102, 0x104)")
     ap.add_argument("--prefill-form", choices=("chunked", "recurrent"), default="chunked",
                     help="prefill workloads: gdn_prefill_chunked (tensor cores) or gdn_prefill (per token)")
     args = ap.parse_args()

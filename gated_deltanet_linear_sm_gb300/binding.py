@@ -22,6 +22,7 @@ GDN_FLAG_ACCEPTED = 2
 GDN_FLAG_QLEN = 4
 GDN_FLAG_TOKEN_ROW = 8
 GDN_FLAG_TIMEOUT = 16
+GDN_SPLIT_NARROW = 0x100     # dims.split flag: 8 V columns per warp (small batches)
 
 
 class gdn_dims(ctypes.Structure):
@@ -74,7 +75,7 @@ EXPORTS = {
                                                        ctypes.c_float, ctypes.c_int, _VP, _VP]),
     "gdn_spec_decode_conv": (ctypes.c_int, [_VP] * 6 + [ctypes.POINTER(gdn_conv_dims)] + [_VP] * 12 +
                              [ctypes.POINTER(gdn_dims), ctypes.c_float, ctypes.c_float, ctypes.c_int, _VP, _VP]),
-    "gdn_spec_decode_split": (ctypes.c_int32, [ctypes.POINTER(gdn_dims)]),
+    "gdn_spec_decode_split": (ctypes.c_int32, [ctypes.POINTER(gdn_dims), ctypes.c_int]),
     "gdn_status_str": (ctypes.c_char_p, [ctypes.c_int]),
     "gdn_version": (ctypes.c_int32, []),
 }
@@ -197,6 +198,10 @@ class PreparedCall:
     def dims(self) -> gdn_dims:
         return self._dims
 
+    @property
+    def state_dtype(self) -> int:
+        return self._state_dtype
+
     def __call__(self, stream=None):
         """Launch on `stream`: a torch.cuda.Stream, a raw cudaStream_t handle
         (int), or None for the current stream."""
@@ -259,8 +264,10 @@ def prepare(q, k, v, a, b, z, A_log, dt_bias, norm_w, state_pool, state_indices,
                         status_ptr=_ptr(status))
 
 
-def chosen_split(dims: gdn_dims) -> int:
-    return int(load_library().gdn_spec_decode_split(ctypes.byref(dims)))
+def chosen_split(dims: gdn_dims, state_dtype: int = BF16) -> int:
+    """The split code gdn_spec_decode uses for these sizes and state dtype
+    (F32 / BF16 / F16)."""
+    return int(load_library().gdn_spec_decode_split(ctypes.byref(dims), int(state_dtype)))
 
 
 def gdn_prefill(q, k, v, a, b, z, A_log, dt_bias, norm_w, state_pool, read_slots, write_slots,

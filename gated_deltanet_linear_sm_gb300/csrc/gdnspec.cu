@@ -36,6 +36,10 @@
 //  * Small batches may split the 8 column blocks of a unit over SPLIT CTAs of
 //    one thread-block cluster (SPLIT = 2, 4, 8); the gated RMSNorm's
 //    mean-square over V is then combined through distributed shared memory.
+//    The narrow layout (NCW = 8) gives each warp 8 columns instead of 16: a
+//    unit's 16 warps run over a 2- or 4-CTA cluster with half the state per
+//    lane and one more butterfly step; it is the automatic choice for an FP32
+//    state with at most 64 units.
 //  * No device-side waits on flags, no traps: bad device data is skipped and
 //    reported through an optional status word.
 //  * Fused convolution (CONV = true, SPLIT = 1): each lane convolves its 12
@@ -66,21 +70,35 @@ namespace {
 constexpr int kK = 128;
 constexpr int kV = 128;
 constexpr int kMaxT = 8;
-constexpr int kColsPerWarp = 16;
-constexpr int kRowsPerLane = 16;
+constexpr int kColsPerWarp = 16;             // the default (wide) warp: 16 V columns ...
+constexpr int kRowsPerLane = 16;             // ... 16 K rows per lane
 constexpr float kQkEps = 1e-6f;              // inside the L2-norm square root
 constexpr float kSoftplusThreshold = 20.0f;  // softplus(x) = x above this
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int64_t kTile = static_cast<int64_t>(kK) * kV;
-// k^ / q^ rows in shared memory: 4 floats of padding after every 16 rows, so
-// that the 8 row groups of a warp (16 rows = 64 B apart) land on distinct
-// banks when each reads its 16-byte chunk
-constexpr int kKPad = kK + kK / 4;
-__host__ __device__ constexpr int kpos(int row) { return row + (row >> 4) * 4; }
-// A lane of row group rg (0..7) holds K rows rg + 8 j, j = 0..15.  k^ / q^ are
-// stored permuted so that those 16 rows are contiguous: row -> 16 (row % 8) +
-// row / 8, then padded as above.
-__host__ __device__ constexpr int kperm(int row) { return kpos((row & 7) * 16 + (row >> 3)); }
+// Lane layout of a warp's block of the state tile.  NCW = V columns per warp:
+// 16 (the default) or 8 (the narrow variant for small batches, where a unit's
+// 16 warps spread over a 2- or 4-CTA cluster).  Lane = cg + (NCW/4) rg holds
+// the 4 consecutive columns of column group cg in the K rows rg + G j, j = 0
+// .. R-1 (G row groups, R = 128 / G rows per lane).  The lane bits above the
+// column group are the row group in both layouts, so the reduce-scatter over
+// lane bits 4, 3, 2 means the same in both.
+template <int NCW>
+struct Lanes {
+    static_assert(NCW == 16 || NCW == 8, "16 or 8 columns per warp");
+    static constexpr int kColGroups = NCW / 4;            // 4 or 2
+    static constexpr int kRowGroups = 32 / kColGroups;    // 8 or 16
+    static constexpr int kRows = kK / kRowGroups;         // 16 or 8
+    // k^ / q^ sit in shared memory permuted so that a lane's rows are
+    // contiguous (row -> R (row % G) + row / G), with 4 floats of padding after
+    // every 16 (NCW = 16) or 32 (NCW = 8) positions: the row groups' 16-byte
+    // chunks then spread evenly over the banks (one wavefront for 8 groups,
+    // two for 16).
+    static constexpr int kPadEvery = NCW == 16 ? 16 : 32;
+    __host__ __device__ static constexpr int pos(int p) { return p + (p / kPadEvery) * 4; }
+    __host__ __device__ static constexpr int perm(int row) { return pos((row % kRowGroups) * kRows + row / kRowGroups); }
+};
+constexpr int kKPad = kK + kK / 4;           // room for either padding
 
 using gdn_internal::Params;
 
@@ -97,13 +115,13 @@ struct alignas(16) Smem {
     long long ws[kMaxT];
 };
 
-template <typename StateT, int SPLIT>
+template <typename StateT, int SPLIT, int NCW = kColsPerWarp>
 struct Config {
-    static constexpr int kWarps = 8 / SPLIT;
+    static constexpr int kWarps = kV / NCW / SPLIT;
     static constexpr int kThreads = 32 * kWarps;
     // each warp stages its 128 x 16 block of a token's state for the tensor store
     static constexpr size_t kStageOffset = (sizeof(Smem) + 127) / 128 * 128;
-    static constexpr size_t kStageElems = static_cast<size_t>(kK) * kColsPerWarp;
+    static constexpr size_t kStageElems = static_cast<size_t>(kK) * NCW;
     // + 128 bytes so that the staging buffers can start on a 128-byte boundary
     static constexpr size_t kSmem = kStageOffset + kWarps * kStageElems * sizeof(StateT) + 128;
 };
@@ -237,6 +255,7 @@ __device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
 // Per-token prologue arithmetic for token t of unit (i, h), one warp: the raw
 // quads are this lane's 4 elements of q, k (key head), v and z (v-head);
 // `ws` is the slot that receives the state after this token (-1: none).
+template <int NCW = kColsPerWarp>
 __device__ __forceinline__ void prologue_token_f(Smem& s, const Params& p, int h, int t, int r, int lane,
                                                  float (&qv)[4], float (&kv)[4], const float (&vv)[4], uint2 zraw,
                                                  long long ws) {
@@ -265,8 +284,8 @@ __device__ __forceinline__ void prologue_token_f(Smem& s, const Params& p, int h
     for (int e = 0; e < 4; ++e) { qv[e] *= rq; kv[e] *= rk; }
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-        s.q[t][kperm(lane * 4 + e)] = qv[e];
-        s.k[t][kperm(lane * 4 + e)] = kv[e];
+        s.q[t][Lanes<NCW>::perm(lane * 4 + e)] = qv[e];
+        s.k[t][Lanes<NCW>::perm(lane * 4 + e)] = kv[e];
     }
     *reinterpret_cast<float4*>(&s.v[t][lane * 4]) = make_float4(vv[0], vv[1], vv[2], vv[3]);
     s.z[t][lane] = zraw;
@@ -281,25 +300,27 @@ __device__ __forceinline__ void prologue_token_f(Smem& s, const Params& p, int h
     }
 }
 
+template <int NCW = kColsPerWarp>
 __device__ __forceinline__ void prologue_token(Smem& s, const Params& p, int h, int t, int r, int lane,
                                                uint2 qraw, uint2 kraw, uint2 vraw, uint2 zraw, long long ws) {
     float qv[4], kv[4], vv[4];
     unpack_bf16x4(qraw, qv);
     unpack_bf16x4(kraw, kv);
     unpack_bf16x4(vraw, vv);
-    prologue_token_f(s, p, h, t, r, lane, qv, kv, vv, zraw, ws);
+    prologue_token_f<NCW>(s, p, h, t, r, lane, qv, kv, vv, zraw, ws);
 }
 
 // One draft token for this lane's 16x4 block: both reductions, the delta rule,
 // the readout into s.o, the state update and (when s.ws[t] names a slot) the
 // slot write.
-template <typename StateT>
-__device__ __forceinline__ void token_step(float (&S)[kRowsPerLane][4], Smem& s, const Params& p, int t, int h,
-                                           int lane, int col0, int row0, int rank, StateT* stage) {
-    const int cgi = lane & 3;
-    const int rg = lane >> 2;
-    const int c_own = rg & 3;          // after the reduce-scatter: my column ...
-    const int d_own = rg >> 2;         // ... and which dot product (0: k, 1: q)
+template <typename StateT, int NCW = kColsPerWarp>
+__device__ __forceinline__ void token_step(float (&S)[Lanes<NCW>::kRows][4], Smem& s, const Params& p, int t,
+                                           int h, int lane, int col0, int row0, int rank, StateT* stage) {
+    using L = Lanes<NCW>;
+    const int cgi = lane % L::kColGroups;
+    const int rg = lane / L::kColGroups;
+    const int c_own = (lane >> 2) & 3; // after the reduce-scatter: my column ...
+    const int d_own = (lane >> 4) & 1; // ... and which dot product (0: k, 1: q)
     const float decay = s.decay[t];
     const float beta = s.beta[t];
     const float kq = s.kq[t];
@@ -309,9 +330,9 @@ __device__ __forceinline__ void token_step(float (&S)[kRowsPerLane][4], Smem& s,
 #pragma unroll
     for (int e = 0; e < 8; ++e) x[e] = 0.f;
 #pragma unroll
-    for (int r4 = 0; r4 < kRowsPerLane / 4; ++r4) {
-        const float4 kk = *reinterpret_cast<const float4*>(&s.k[t][kpos(row0 + 4 * r4)]);
-        const float4 qq = *reinterpret_cast<const float4*>(&s.q[t][kpos(row0 + 4 * r4)]);
+    for (int r4 = 0; r4 < L::kRows / 4; ++r4) {
+        const float4 kk = *reinterpret_cast<const float4*>(&s.k[t][L::pos(row0 + 4 * r4)]);
+        const float4 qq = *reinterpret_cast<const float4*>(&s.q[t][L::pos(row0 + 4 * r4)]);
         const float kr[4] = {kk.x, kk.y, kk.z, kk.w};
         const float qr[4] = {qq.x, qq.y, qq.z, qq.w};
 #pragma unroll
@@ -326,8 +347,11 @@ __device__ __forceinline__ void token_step(float (&S)[kRowsPerLane][4], Smem& s,
                 upk2(xq, x[4 + c], x[5 + c]);
             }
     }
-    // reduce-scatter over the 8 row groups (lane bits 4, 3, 2): afterwards
-    // lane (cg, rg) holds the full sum of value index rg = 4 d + c
+    // reduce-scatter over the row groups on lane bits 4, 3, 2: afterwards the
+    // lane holds the sum of value index 4 d + c = (lane >> 2) & 7 (d = 0: k,
+    // 1: q; c: column within its group) over those groups; with 16 row groups
+    // (NCW = 8) lane bit 1 is a row-group bit too and one more step completes
+    // the sum on both lanes of the pair
     float y[4];
     {
         const bool hi = (lane >> 4) & 1;
@@ -355,6 +379,7 @@ __device__ __forceinline__ void token_step(float (&S)[kRowsPerLane][4], Smem& s,
         const float keep = hi ? z2[1] : z2[0];
         dot = keep + __shfl_xor_sync(kFull, send, 4);
     }
+    if constexpr (NCW == 8) dot += __shfl_xor_sync(kFull, dot, 2);
     // delta rule on the k lanes; readout on the q lanes
     const float vp = beta * (s.v[t][col0 + c_own] - decay * dot);   // valid where d_own == 0
     const float vp_pair = __shfl_xor_sync(kFull, vp, 16);
@@ -365,8 +390,8 @@ __device__ __forceinline__ void token_step(float (&S)[kRowsPerLane][4], Smem& s,
 
     // S <- e^g S + k^ v'^T
 #pragma unroll
-    for (int r4 = 0; r4 < kRowsPerLane / 4; ++r4) {
-        const float4 kk = *reinterpret_cast<const float4*>(&s.k[t][kpos(row0 + 4 * r4)]);
+    for (int r4 = 0; r4 < L::kRows / 4; ++r4) {
+        const float4 kk = *reinterpret_cast<const float4*>(&s.k[t][L::pos(row0 + 4 * r4)]);
         const float kr[4] = {kk.x, kk.y, kk.z, kk.w};
 #pragma unroll
         for (int rr = 0; rr < 4; ++rr)
@@ -391,8 +416,8 @@ __device__ __forceinline__ void token_step(float (&S)[kRowsPerLane][4], Smem& s,
             if (lane == 0) tma_wait_read();
             __syncwarp();
 #pragma unroll
-            for (int r = 0; r < kRowsPerLane; ++r)
-                StateIO<StateT>::stage4(stage + (rg + 8 * r) * kColsPerWarp + 4 * cgi, S[r]);
+            for (int r = 0; r < L::kRows; ++r)
+                StateIO<StateT>::stage4(stage + (rg + L::kRowGroups * r) * NCW + 4 * cgi, S[r]);
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             __syncwarp();
             if (lane == 0)
@@ -400,7 +425,8 @@ __device__ __forceinline__ void token_step(float (&S)[kRowsPerLane][4], Smem& s,
         } else {
             StateT* d = static_cast<StateT*>(p.pool) + (ws * p.H_v + h) * kTile + col0;
 #pragma unroll
-            for (int r = 0; r < kRowsPerLane; ++r) StateIO<StateT>::store4(d + static_cast<int64_t>(rg + 8 * r) * kV, S[r]);
+            for (int r = 0; r < L::kRows; ++r)
+                StateIO<StateT>::store4(d + static_cast<int64_t>(rg + L::kRowGroups * r) * kV, S[r]);
         }
     }
 }
@@ -409,9 +435,8 @@ __device__ __forceinline__ void token_step(float (&S)[kRowsPerLane][4], Smem& s,
 // rsqrt(mean(o^2) + eps) * w * silu(z), written at the rows in s.row.  With
 // SPLIT > 1 the mean-square is combined across the cluster through
 // distributed shared memory.
-template <int SPLIT>
+template <int SPLIT, int W = 8 / SPLIT>
 __device__ __forceinline__ void epilogue(Smem& s, const Params& p, int h, int n, int warp, int lane, int rank) {
-    constexpr int W = 8 / SPLIT;
     constexpr int CW = kV / SPLIT;  // V columns of this CTA
     const bool gated = p.z != nullptr;
     if (SPLIT > 1 && gated) {
@@ -565,11 +590,12 @@ __device__ __forceinline__ void conv_token(const Params& p, int bos, int t, cons
 // ---- the speculative decode kernel -------------------------------------------------
 //
 // Grid: one CTA per (unit, column slice); SPLIT CTAs of a unit form one cluster.
-// Block: 8 / SPLIT warps, each owning 16 of the unit's 128 V columns.
-template <typename StateT, int SPLIT, bool CONV = false>
-__global__ void __launch_bounds__(Config<StateT, SPLIT>::kThreads, 2 * SPLIT)
+// Block: 128 / NCW / SPLIT warps, each owning NCW of the unit's 128 V columns.
+template <typename StateT, int SPLIT, bool CONV = false, int NCW = kColsPerWarp>
+__global__ void __launch_bounds__(Config<StateT, SPLIT, NCW>::kThreads, NCW == kColsPerWarp ? 2 * SPLIT : SPLIT)
 gdn_spec_decode_kernel(const __grid_constant__ Params p) {
-    using C = Config<StateT, SPLIT>;
+    using C = Config<StateT, SPLIT, NCW>;
+    using L = Lanes<NCW>;
     constexpr int W = C::kWarps;
     extern __shared__ __align__(128) unsigned char smem_raw[];
     Smem& s = *reinterpret_cast<Smem*>(smem_raw);
@@ -580,11 +606,11 @@ gdn_spec_decode_kernel(const __grid_constant__ Params p) {
     const int unit = static_cast<int>(blockIdx.x / SPLIT);
     const int i = unit / p.H_v;
     const int h = unit - i * p.H_v;
-    const int cgi = lane & 3;        // column group: 4 consecutive columns
-    const int rg = lane >> 2;        // row group: 16 consecutive K rows
-    const int wg = rank * W + warp;  // this warp's 16-column block (0..7)
-    const int col0 = wg * kColsPerWarp + cgi * 4;
-    const int row0 = rg * kRowsPerLane;
+    const int cgi = lane % L::kColGroups;  // column group: 4 consecutive columns
+    const int rg = lane / L::kColGroups;   // row group: K rows rg + G j
+    const int wg = rank * W + warp;        // this warp's NCW-column block
+    const int col0 = wg * NCW + cgi * 4;
+    const int row0 = rg * L::kRows;        // where those rows sit in the permuted k^ / q^
 
     // Launched with programmatic stream serialization: this CTA may become
     // resident while the previous kernel in the stream is still running.  It
@@ -634,13 +660,13 @@ gdn_spec_decode_kernel(const __grid_constant__ Params p) {
         }
     }
 
-    // ---- load this lane's 16x4 block of the state tile (FP32 in registers):
-    //      rows rg + 8 r, columns col0 .. col0 + 3 ----
+    // ---- load this lane's R x 4 block of the state tile (FP32 in registers):
+    //      rows rg + G r, columns col0 .. col0 + 3 ----
     const StateT* src = static_cast<const StateT*>(p.pool) + (rs * p.H_v + h) * kTile;
-    float S[kRowsPerLane][4];
+    float S[L::kRows][4];
 #pragma unroll
-    for (int r = 0; r < kRowsPerLane; ++r)
-        StateIO<StateT>::load4(src + static_cast<int64_t>(rg + 8 * r) * kV + col0, S[r]);
+    for (int r = 0; r < L::kRows; ++r)
+        StateIO<StateT>::load4(src + static_cast<int64_t>(rg + L::kRowGroups * r) * kV + col0, S[r]);
 
     // ---- per-token prologue: gather rows, gates, normalised q / k, v, z ----
     const int kh = h / p.group;
@@ -648,7 +674,7 @@ gdn_spec_decode_kernel(const __grid_constant__ Params p) {
     int bad = 0;
 
 #pragma unroll
-    for (int j = 0; j < SPLIT; ++j) {                          // W * SPLIT = 8 >= q_len
+    for (int j = 0; j < (kMaxT + W - 1) / W; ++j) {            // warp w: tokens w, w + W, ...
         const int t = warp + j * W;
         if (t < q_len) {
             const int n = bos + t;
@@ -668,11 +694,11 @@ gdn_spec_decode_kernel(const __grid_constant__ Params p) {
                     const uint2 zraw = p.z != nullptr
                                            ? ldg_quad(p.z + r * p.z_stride + static_cast<int64_t>(h) * kV + lane * 4)
                                            : make_uint2(0, 0);
-                    prologue_token_f(s, p, h, t, r, lane, y[0], y[1], y[2], zraw, ws);
+                    prologue_token_f<NCW>(s, p, h, t, r, lane, y[0], y[1], y[2], zraw, ws);
                 } else {
                     uint2 qraw, kraw, vraw, zraw;
                     load_token_quads(p, r, kh, h, lane, qraw, kraw, vraw, zraw);
-                    prologue_token(s, p, h, t, r, lane, qraw, kraw, vraw, zraw, ws);
+                    prologue_token<NCW>(s, p, h, t, r, lane, qraw, kraw, vraw, zraw, ws);
                 }
             }
         }
@@ -714,11 +740,11 @@ gdn_spec_decode_kernel(const __grid_constant__ Params p) {
     StateT* stage = reinterpret_cast<StateT*>(smem_raw + C::kStageOffset +
                                               ((128u - (smem_addr(smem_raw) & 127u)) & 127u)) +
                     warp * C::kStageElems;
-    for (int t = 0; t < q_len; ++t) token_step<StateT>(S, s, p, t, h, lane, col0, row0, rank, stage);
+    for (int t = 0; t < q_len; ++t) token_step<StateT, NCW>(S, s, p, t, h, lane, col0, row0, rank, stage);
 
     // ---- gated RMSNorm epilogue ----
     __syncthreads();                                           // s.o of this CTA complete
-    epilogue<SPLIT>(s, p, h, q_len, warp, lane, rank);
+    epilogue<SPLIT, W>(s, p, h, q_len, warp, lane, rank);
     if (lane == 0) tma_wait_all();                              // the slot writes have landed
 }
 
@@ -787,10 +813,10 @@ __global__ void __launch_bounds__(256, 2) gdn_prefill_kernel(const Params p) {
 
 // ---- host side ----------------------------------------------------------------
 
-template <typename StateT, int SPLIT, bool CONV = false>
+template <typename StateT, int SPLIT, bool CONV = false, int NCW = kColsPerWarp>
 cudaError_t launch(const Params& p, int64_t units, cudaStream_t stream) {
-    using C = Config<StateT, SPLIT>;
-    auto kernel = gdn_spec_decode_kernel<StateT, SPLIT, CONV>;
+    using C = Config<StateT, SPLIT, NCW>;
+    auto kernel = gdn_spec_decode_kernel<StateT, SPLIT, CONV, NCW>;
     if (C::kSmem > 48 * 1024) {
         // opt in to more than 48 KB of dynamic shared memory, once per device
         static bool done[64] = {false};
@@ -830,6 +856,8 @@ cudaError_t launch_split(const Params& p, int64_t units, int split, cudaStream_t
     case 1: return launch<StateT, 1>(p, units, stream);
     case 2: return launch<StateT, 2>(p, units, stream);
     case 4: return launch<StateT, 4>(p, units, stream);
+    case GDN_SPLIT_NARROW | 2: return launch<StateT, 2, false, 8>(p, units, stream);
+    case GDN_SPLIT_NARROW | 4: return launch<StateT, 4, false, 8>(p, units, stream);
     default: return launch<StateT, 8>(p, units, stream);
     }
 }
@@ -848,11 +876,12 @@ cudaError_t launch_prefill(const Params& p, int64_t units, cudaStream_t stream) 
 bool aligned(const void* ptr, uintptr_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }
 
 // The state pool as a 2-D tensor for the decode kernel's per-warp tensor
-// stores: rows = slots * H_v * K, columns = V, box = 128 rows x 16 columns.
+// stores: rows = slots * H_v * K, columns = V, box = 128 rows x `cols` columns
+// (the columns a warp owns: 16, or 8 in the narrow layout).
 // cuTensorMapEncodeTiled is reached through the runtime's driver entry point
 // (no link against the driver library); maps are cached per host thread for
 // the last few pools, so a steady stream of calls encodes nothing.
-gdn_status make_pool_map(Params& p, void* pool, int64_t num_slots, int32_t H_v, gdn_dtype dt) {
+gdn_status make_pool_map(Params& p, void* pool, int64_t num_slots, int32_t H_v, gdn_dtype dt, int cols) {
     using Encode = PFN_cuTensorMapEncodeTiled_v12000;
     static const Encode encode = [] {
         void* fn = nullptr;
@@ -869,20 +898,20 @@ gdn_status make_pool_map(Params& p, void* pool, int64_t num_slots, int32_t H_v, 
     struct Entry {
         const void* pool;
         int64_t rows;
-        int dt;
+        int dt, cols;
         CUtensorMap map;
     };
     thread_local Entry cache[4] = {};
     thread_local int next = 0;
     for (const Entry& e : cache)
-        if (e.pool == pool && e.rows == rows && e.dt == dt) {
+        if (e.pool == pool && e.rows == rows && e.dt == dt && e.cols == cols) {
             p.pool_map = e.map;
             return GDN_OK;
         }
     const size_t elem = dt == GDN_F32 ? 4 : 2;
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kV), static_cast<cuuint64_t>(rows)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kV * elem)};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kColsPerWarp), static_cast<cuuint32_t>(kK)};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(cols), static_cast<cuuint32_t>(kK)};
     const cuuint32_t estr[2] = {1, 1};
     const CUtensorMapDataType type = dt == GDN_F32    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
                                      : dt == GDN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
@@ -892,16 +921,22 @@ gdn_status make_pool_map(Params& p, void* pool, int64_t num_slots, int32_t H_v, 
                CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return GDN_ERR_CUDA;
-    cache[next] = Entry{pool, rows, static_cast<int>(dt), map};
+    cache[next] = Entry{pool, rows, static_cast<int>(dt), cols, map};
     next = (next + 1) % 4;
     p.pool_map = map;
     return GDN_OK;
 }
 
-// One CTA per unit at every batch size measured (4 to 128 sequences of 16
-// v-heads): splitting a unit's columns over a cluster shortens no per-token
-// chain and adds cluster barriers, so the default is 1.
-int choose_split(int64_t /*units*/) { return 1; }
+// One CTA per unit, each warp owning 16 V columns, at every batch size
+// measured (4 to 256 sequences of 16 v-heads) but one: an FP32 state with at
+// most 64 units (4 sequences of 16 v-heads) runs the narrow layout over 2-CTA
+// clusters (BS=4: 13.9 -> 11.6 us).  Splitting the 16-column warps over a
+// cluster shortens no per-token chain and adds cluster barriers; narrow warps
+// with 16-bit states store 16-byte rows, whose tensor stores cost more than
+// the shorter chain saves.
+int choose_split(int64_t units, gdn_dtype dt) {
+    return (dt == GDN_F32 && units <= 64) ? (GDN_SPLIT_NARROW | 2) : 1;
+}
 
 gdn_status check_dims(const gdn_dims* d) {
     if (d == nullptr) return GDN_ERR_NULL_ARG;
@@ -913,7 +948,8 @@ gdn_status check_dims(const gdn_dims* d) {
         d->z_stride < 0 || d->out_stride < 0)
         return GDN_ERR_BAD_SHAPE;
     if (d->K != kK || d->V != kV) return GDN_ERR_UNSUPPORTED;
-    if (!(d->split == 0 || d->split == 1 || d->split == 2 || d->split == 4 || d->split == 8))
+    if (!(d->split == 0 || d->split == 1 || d->split == 2 || d->split == 4 || d->split == 8 ||
+          d->split == (GDN_SPLIT_NARROW | 2) || d->split == (GDN_SPLIT_NARROW | 4)))
         return GDN_ERR_UNSUPPORTED;
     if (static_cast<int64_t>(d->batch) * d->H_v * 8 > 0x7fffffffLL) return GDN_ERR_BAD_SHAPE;
     return GDN_OK;
@@ -1035,10 +1071,11 @@ gdn_status gdn_spec_decode(const void* q, const void* k, const void* v, const vo
     p.idx = state_indices;
     p.num_acc = num_accepted;
     p.sti = spec_token_indx;
-    const gdn_status ms = make_pool_map(p, state_pool, dims->num_slots, dims->H_v, state_dtype);
-    if (ms != GDN_OK) return ms;
     const int64_t units = static_cast<int64_t>(dims->batch) * dims->H_v;
-    const int split = dims->split ? dims->split : choose_split(units);
+    const int split = dims->split ? dims->split : choose_split(units, state_dtype);
+    const gdn_status ms = make_pool_map(p, state_pool, dims->num_slots, dims->H_v, state_dtype,
+                                        (split & GDN_SPLIT_NARROW) ? 8 : kColsPerWarp);
+    if (ms != GDN_OK) return ms;
     const cudaError_t err =
         by_state_dtype<DecodeLauncher>(state_dtype, p, units, split, reinterpret_cast<cudaStream_t>(stream));
     return err == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
@@ -1076,7 +1113,7 @@ gdn_status gdn_spec_decode_conv(const void* x, const void* conv_weight, const vo
     p.idx = state_indices;
     p.num_acc = num_accepted;
     p.sti = spec_token_indx;
-    const gdn_status ms = make_pool_map(p, state_pool, dims->num_slots, dims->H_v, state_dtype);
+    const gdn_status ms = make_pool_map(p, state_pool, dims->num_slots, dims->H_v, state_dtype, kColsPerWarp);
     if (ms != GDN_OK) return ms;
     p.conv_dim = 2 * dims->H_k * kK + dims->H_v * kV;
     p.x = static_cast<const __nv_bfloat16*>(x);
@@ -1141,10 +1178,11 @@ gdn_status gdn_prefill_chunked(const void* q, const void* k, const void* v, cons
     return err == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
-int32_t gdn_spec_decode_split(const gdn_dims* dims) {
+int32_t gdn_spec_decode_split(const gdn_dims* dims, gdn_dtype state_dtype) {
     if (check_dims(dims) != GDN_OK) return 0;
+    if (state_dtype != GDN_F32 && state_dtype != GDN_BF16 && state_dtype != GDN_F16) return 0;
     if (dims->split) return dims->split;
-    return choose_split(static_cast<int64_t>(dims->batch) * dims->H_v);
+    return choose_split(static_cast<int64_t>(dims->batch) * dims->H_v, state_dtype);
 }
 
 const char* gdn_status_str(gdn_status status) {

@@ -82,6 +82,15 @@ typedef enum { GDN_F32 = 0, GDN_BF16 = 1, GDN_F16 = 2 } gdn_dtype;
 #define GDN_FLAG_TIMEOUT    16 /* gdn_prefill_chunked only: a wait on the tensor cores ran past its
                                   bound; that sequence's outputs and final state are incomplete */
 
+/*
+ * dims->split flag: each warp of the decode step owns 8 of a unit's 128 V
+ * columns instead of 16, so a unit runs on 16 warps with half the state per
+ * lane and half the work per token.  Meant for small batches, where most SMs
+ * would otherwise idle: the unit's warps spread over a 2- or 4-CTA cluster.
+ * Same results up to FP32 rounding order.
+ */
+#define GDN_SPLIT_NARROW 0x100
+
 /* Opaque CUDA stream handle; the same type as cudaStream_t (NULL = legacy default stream). */
 typedef struct CUstream_st* gdn_stream_t;
 
@@ -101,7 +110,10 @@ typedef struct {
        v_stride = 2*H_k*K + H_v*V. */
     int64_t q_stride, k_stride, v_stride, a_stride, b_stride, z_stride, out_stride;
     int32_t split;        /* CTAs per (sequence, v-head), one thread-block cluster:
-                             0 = chosen from the batch size; else 1, 2, 4 or 8 */
+                             0 = chosen from the batch size; else 1, 2, 4 or 8
+                             (each warp owns 16 V columns), or GDN_SPLIT_NARROW
+                             | 2 or | 4 (each warp owns 8 V columns: 16 warps
+                             per unit over 2 or 4 CTAs) */
     int32_t reserved;     /* must be 0 */
 } gdn_dims;
 
@@ -295,11 +307,12 @@ GDNSPEC_API gdn_status gdn_spec_decode_conv(
     int32_t* status_word, gdn_stream_t stream);
 
 /*
- * The CTAs per (sequence, v-head) that gdn_spec_decode would use for these
- * sizes when dims->split == 0 (1, 2, 4 or 8), or 0 for invalid dims.  Host
- * only; queries the current device's SM count.
+ * The split code that gdn_spec_decode would use for these sizes and state
+ * dtype (dims->split itself when it is not 0; else 1, or GDN_SPLIT_NARROW | 2
+ * for an FP32 state with batch * H_v <= 64), or 0 for invalid dims or dtype.
+ * Host only; reads no device state.
  */
-GDNSPEC_API int32_t gdn_spec_decode_split(const gdn_dims* dims);
+GDNSPEC_API int32_t gdn_spec_decode_split(const gdn_dims* dims, gdn_dtype state_dtype);
 
 /* Static English text for a status code (never NULL). */
 GDNSPEC_API const char* gdn_status_str(gdn_status status);

@@ -96,7 +96,8 @@ def _call(lib, dims, *, ptr=0x1000, z=0x1000, w=0x1000, state_dtype=0):
 @pytest.mark.parametrize("over,code", [
     (dict(K=64), 3), (dict(V=256), 3), (dict(H_v=12, H_k=8), 2), (dict(max_T=9), 2),
     (dict(max_T=0), 2), (dict(spec_stride=0), 2), (dict(batch=-1), 2), (dict(num_slots=0), 2),
-    (dict(split=3), 3), (dict(reserved=1), 2), (dict(q_stride=-4), 2),
+    (dict(split=3), 3), (dict(split=0x101), 3), (dict(split=0x108), 3), (dict(split=0x100), 3),
+    (dict(reserved=1), 2), (dict(q_stride=-4), 2),
 ])
 def test_bad_dims_rejected(lib, over, code):
     assert _call(lib, _dims(**over)) == code
@@ -117,9 +118,20 @@ def test_empty_batch_is_a_no_op(lib):
 
 
 def test_explicit_split_is_reported(lib):
-    for s in (1, 2, 4, 8):
+    for s in (1, 2, 4, 8, binding.GDN_SPLIT_NARROW | 2, binding.GDN_SPLIT_NARROW | 4):
         assert binding.chosen_split(_dims(split=s)) == s
     assert binding.chosen_split(_dims(K=64)) == 0
+    assert binding.chosen_split(_dims(), 7) == 0
+
+
+def test_automatic_split():
+    """FP32 state with at most 64 units: the narrow layout over 2-CTA
+    clusters; everything else one CTA per unit."""
+    N2 = binding.GDN_SPLIT_NARROW | 2
+    assert binding.chosen_split(_dims(batch=4, H_v=16), binding.F32) == N2
+    assert binding.chosen_split(_dims(batch=5, H_v=16), binding.F32) == 1
+    assert binding.chosen_split(_dims(batch=4, H_v=16), binding.BF16) == 1
+    assert binding.chosen_split(_dims(batch=4, H_v=16), binding.F16) == 1
 
 
 def _cdims(**over):
@@ -151,6 +163,7 @@ def test_conv_bad_pointers_rejected(lib):
     assert _call_conv(lib, _dims(), _cdims(), ptr=0) == 1        # NULL tensors
     assert _call_conv(lib, _dims(), _cdims(), bias=0x1002) == 4   # bias not 8-byte aligned
     assert _call_conv(lib, _dims(split=2), _cdims()) == 3         # the fused path has no split
+    assert _call_conv(lib, _dims(split=binding.GDN_SPLIT_NARROW | 2), _cdims()) == 3
     assert _call_conv(lib, _dims(batch=0), _cdims(), ptr=0) == 0  # empty batch: nothing launched
     assert lib.gdn_spec_decode_conv(*([None] * 6), None, *([None] * 12), ctypes.byref(_dims()), 0.1, 1e-5, 0,
                                     None, None) == 1

@@ -17,7 +17,7 @@ from tests.gpu_util import (OUT_SENTINEL, active_rows, compare, make_pool, run_g
 
 pytestmark = pytest.mark.gpu
 
-SPLITS = (1, 2, 4, 8)
+SPLITS = (1, 2, 4, 8, 0x102, 0x104)      # 0x100: GDN_SPLIT_NARROW (8 columns per warp)
 
 
 def _invariants(case, pool_before, pool_after, out):
