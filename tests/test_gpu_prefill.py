@@ -199,3 +199,15 @@ def test_empty_prompts_touch_nothing(entry):
     out, pool, st, ref, host = _run(entry, case, reads, writes)
     assert np.array_equal(to_host_bits(pool)[[10, 12]], host[[10, 12]])
     _check(entry, case, out, pool, st, ref, host, np.array([-1, 11, -1, 13], np.int32))
+
+
+@pytest.mark.parametrize("bs,L", [(4, 1024), (32, 256)])
+@pytest.mark.parametrize("entry", list(ENTRIES))
+def test_benchmark_workloads_full_size(entry, bs, L):
+    """The benchmark's prefill workloads at full size (H_k = 2, H_v = 16, bf16
+    state, every prompt L tokens), started from slots and stored to other
+    slots, every sequence compared."""
+    case = synth.make_case(batch=bs, H_k=2, H_v=16, T=L, state_dtype=synth.BF16, num_slots=max(4 * bs, 64),
+                           spec_stride=1, q_lens=[L] * bs, acc=[1] * bs, seed=59 + bs)
+    reads, writes = _slots(case, 6, zero_every=10 ** 6, skip_every=10 ** 6)
+    _check(entry, case, *_run(entry, case, reads, writes), writes)
