@@ -48,7 +48,8 @@
 extern "C" {
 #endif
 
-#define GDNSPEC_VERSION 1
+/* 2: gdn_spec_decode_split takes the state dtype; dims->split accepts GDN_SPLIT_NARROW */
+#define GDNSPEC_VERSION 2
 
 #if defined(__GNUC__)
 #define GDNSPEC_API __attribute__((visibility("default")))
