@@ -31,7 +31,6 @@ Layouts (row-major, contiguous):
 from __future__ import annotations
 
 import dataclasses
-import math
 
 import numpy as np
 

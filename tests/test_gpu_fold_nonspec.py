@@ -21,8 +21,8 @@ import torch
 import gated_deltanet_linear_sm_gb300 as gdn
 from gated_deltanet_linear_sm_gb300 import synth
 from oracle import oracle as orc
-from tests.gpu_util import device_tensors, make_pool, t_bf16, to_host_bits
-from tests.util import bf16_values, initial_pool, rel_l2, state_values
+from tests.gpu_util import device_tensors, make_pool, to_host_bits
+from tests.util import bf16_values, rel_l2, state_values
 
 pytestmark = pytest.mark.gpu
 

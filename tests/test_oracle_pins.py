@@ -17,7 +17,7 @@ import torch
 from gated_deltanet_linear_sm_gb300 import synth
 from oracle import oracle as orc
 from tests import ref_numpy
-from tests.util import (as_bf16_exact, bf16_bits, bf16_values, f16_values, initial_pool,
+from tests.util import (as_bf16_exact, bf16_values, f16_values, initial_pool,
                         one_sequence, rel_l2, state_values)
 
 K = V = 128
