@@ -7,6 +7,8 @@ and which bytes stay untouched is compared bit for bit.
 """
 from __future__ import annotations
 
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -14,6 +16,7 @@ import torch
 from gated_deltanet_linear_sm_gb300 import synth
 from tests.gpu_util import (OUT_SENTINEL, active_rows, compare, make_pool, run_gpu, to_host_bits,
                             written_slots)
+from tests.util import bf16_bits, bf16_values
 
 pytestmark = pytest.mark.gpu
 
@@ -248,3 +251,29 @@ def test_deterministic(cuda_device):
         torch.cuda.synchronize()
         r.append((out.view(torch.int16).clone(), pool.view(torch.int16).clone()))
     assert torch.equal(r[0][0], r[1][0]) and torch.equal(r[0][1], r[1][1])
+
+
+@pytest.mark.parametrize("split", [0, 0x102])
+def test_gate_and_input_extremes(cuda_device, split):
+    """Each input at the end of its range, against the oracle: a + dt_bias above
+    the softplus threshold (heads 0-3), per-token decays that underflow to 0
+    (heads 4-7) or stay within 1e-4 of 1 (heads 8-11), beta saturated at 1 and
+    at ~0 (heads 12-15, alternate tokens), output gates z at +-30, a zero q and
+    k row (the L2-norm epsilon alone) and a state pool of std 30."""
+    case = synth.make_case(batch=6, H_k=2, H_v=16, T=8, state_dtype=synth.F32, num_slots=128, seed=29)
+    a, b, z = bf16_values(case.a), bf16_values(case.b), bf16_values(case.z)
+    q, k = bf16_values(case.q), bf16_values(case.k)
+    A_log = case.A_log.copy()
+    a[:, 0:4] = 30.0
+    A_log[4:8] = np.log(400.0)
+    A_log[8:12] = np.log(1e-4)
+    b[0::2, 12:16] = 40.0
+    b[1::2, 12:16] = -40.0
+    z[:, 0:8, :64] = 30.0
+    z[:, 8:16, 64:] = -30.0
+    q[0, 0] = 0.0
+    k[0, 0] = 0.0
+    ext = dataclasses.replace(case, a=bf16_bits(a), b=bf16_bits(b), z=bf16_bits(z), q=bf16_bits(q),
+                              k=bf16_bits(k), A_log=A_log.astype(np.float32), pool_std=30.0)
+    m = _full_check(ext, cuda_device, split)
+    assert m["out_rel_l2"] < 5e-4

@@ -17,6 +17,7 @@ estimate; narrow states keep atol = rtol = 3e-2.
 """
 from __future__ import annotations
 
+import dataclasses
 import os
 
 import numpy as np
@@ -27,7 +28,7 @@ import gated_deltanet_linear_sm_gb300 as gdn
 from gated_deltanet_linear_sm_gb300 import synth
 from oracle import oracle as orc
 from tests.gpu_util import OUT_SENTINEL, device_tensors, make_pool, to_host_bits
-from tests.util import bf16_values, rel_l2, state_values
+from tests.util import bf16_bits, bf16_values, rel_l2, state_values
 
 pytestmark = pytest.mark.gpu
 
@@ -211,3 +212,24 @@ def test_benchmark_workloads_full_size(entry, bs, L):
                            spec_stride=1, q_lens=[L] * bs, acc=[1] * bs, seed=59 + bs)
     reads, writes = _slots(case, 6, zero_every=10 ** 6, skip_every=10 ** 6)
     _check(entry, case, *_run(entry, case, reads, writes), writes)
+
+
+@pytest.mark.parametrize("entry", list(ENTRIES))
+def test_input_extremes(entry):
+    """a + dt_bias above the softplus threshold (heads 0-3), beta saturated at 1
+    and ~0 on alternate tokens, gates z at +-30, and rows whose q or k is zero
+    (the L2-norm epsilon alone), across a chunk boundary."""
+    case = _case([70, 5], synth.F32, H_k=1, H_v=8, seed=60)
+    a, b, z = bf16_values(case.a), bf16_values(case.b), bf16_values(case.z)
+    q, k = bf16_values(case.q), bf16_values(case.k)
+    a[:, 0:4] = 30.0
+    b[0::2, 4:8] = 40.0
+    b[1::2, 4:8] = -40.0
+    z[:, :, :64] = 30.0
+    z[:, :, 64:] = -30.0
+    q[3] = 0.0
+    k[10] = 0.0
+    k[64] = 0.0
+    ext = dataclasses.replace(case, a=bf16_bits(a), b=bf16_bits(b), z=bf16_bits(z), q=bf16_bits(q), k=bf16_bits(k))
+    reads, writes = _slots(ext, 7, zero_every=10 ** 6, skip_every=10 ** 6)
+    _check(entry, ext, *_run(entry, ext, reads, writes), writes)
