@@ -56,6 +56,10 @@ for _bs, _L in ((4, 1024), (32, 256)):
     WORKLOADS[f"prefill_bs{_bs}_l{_L}_bf16"] = (
         f"prefill: {_bs} prompts x {_L} tokens, H_k=2, H_v=16, K=V=128, bf16 state read from and written to a slot",
         dict(prefill=True, bs=_bs, L=_L))
+for _T in (1, 2, 4):     # shallower drafts (the T = 4 point is the BS=32 decode-batch shape)
+    WORKLOADS[f"bs32_t{_T}_bf16"] = (
+        f"BS=32, H_k=2, H_v=16, K=V=128, T={_T}, bf16 state, acceptance U{{0..{_T}}}, 4096-slot (2 GiB) pool",
+        dict(bs=32, sd="bf16", T=_T))
 WORKLOADS["bs32_t8_bf16_conv"] = (
     "BS=32, H_k=2, H_v=16, K=V=128, T=8, bf16 state, acceptance U{0..8}, 4096-slot pool, with the width-4 "
     "causal convolution and its rewind fused in front (bf16 conv slots, 2 per sequence per set)",
@@ -75,9 +79,9 @@ def make_case(name, seed):
     if spec.get("large"):
         return synth.large(seed, num_slots=N_SETS * 256 * 8)
     sd = {"bf16": synth.BF16, "f32": synth.F32}[spec["sd"]]
-    bs = spec["bs"]
-    ns = max(synth.sweep_num_slots(bs, 8, sd), N_SETS * bs * 8)
-    return synth.sweep(bs, sd, seed=seed, num_slots=ns)
+    bs, T = spec["bs"], spec.get("T", 8)
+    ns = max(synth.sweep_num_slots(bs, T, sd), N_SETS * bs * T)
+    return synth.sweep(bs, sd, T=T, seed=seed, num_slots=ns)
 
 
 # ---------------------------------------------------------------------------
@@ -384,7 +388,7 @@ def run_ours(args, rank, world, local_rank):
     dt_bias_d, norm_w_d = bf(case.dt_bias), bf(case.norm_w)
     for s in range(N_SETS):
         c = case if s == 0 else synth.make_case(
-            batch=case.batch, H_k=case.H_k, H_v=case.H_v, T=8, state_dtype=case.state_dtype,
+            batch=case.batch, H_k=case.H_k, H_v=case.H_v, T=case.spec_stride, state_dtype=case.state_dtype,
             num_slots=case.num_slots, acc=case.num_accepted, seed=100 * rank + s)
         hb = host_bytes(c, sets[s]).pin_memory()
         db = hb.to(dev)
