@@ -40,9 +40,10 @@
  *     o    = S^T q^                              (readout)
  * with S a K x V matrix held as double.  The pages name the inputs and the
  * steps but do not print the formulas; the forms above are the standard
- * gated delta rule those names denote, and every reading taken is listed in
- * the design notes.  Readings used here: softplus(x) = x above the threshold
- * 20 (beta = 1); qk_eps = 1e-6 inside the square root; state layout
+ * gated delta rule those names denote.  Readings used here: softplus(x) = x
+ * above the threshold 20 (beta = 1) and qk_eps = 1e-6 inside the square root
+ * (parity unpinned for these two constants, which the pages do not fix; the
+ * forms they enter are pinned); state layout
  * [slot, H_v, K, V] with V contiguous; a padded read slot (< 0) skips the
  * sequence; a padded write slot skips only that write; the carried state is
  * never rounded, only the copy written to a slot.
