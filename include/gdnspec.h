@@ -230,7 +230,7 @@ GDNSPEC_API gdn_status gdn_prefill(
  * Arguments, layouts, the caller contract and the status bits are those of
  * gdn_prefill; in addition GDN_FLAG_TIMEOUT reports a tensor-core wait that
  * ran past its bound.  One CTA per (sequence, v-head) holding the whole
- * 512-column tensor memory of its SM; ~212 KB of shared memory.
+ * 512-column tensor memory of its SM; ~214 KiB of shared memory.
  * Asynchronous on `stream`, allocates nothing.
  */
 GDNSPEC_API gdn_status gdn_prefill_chunked(
