@@ -135,6 +135,31 @@ def _check(t, name, dtype, device):
         raise ValueError(f"{name}: expected device {device}, got {t.device}")
 
 
+def check_shapes(q, k, v, a, b, z, A_log, dt_bias, norm_w, out=None):
+    """Sizes of the token and parameter tensors against each other, checked
+    before anything else (device, dtype) so that no call with a short buffer
+    reaches the library: q, k [N, H_k, K]; v (and z, out) [N, H_v, V]; a, b
+    [N, H_v]; A_log, dt_bias [H_v]; norm_w [V].  Raises ValueError."""
+    if q.dim() != 3 or k.shape != q.shape:
+        raise ValueError(f"expected q, k [N, H_k, K]; got q {tuple(q.shape)}, k {tuple(k.shape)}")
+    N = q.shape[0]
+    if v.dim() != 3 or v.shape[0] != N:
+        raise ValueError(f"expected v [N={N}, H_v, V]; got {tuple(v.shape)}")
+    H_v, V = v.shape[1], v.shape[2]
+    for t, n in ((a, "a"), (b, "b")):
+        if tuple(t.shape) != (N, H_v):
+            raise ValueError(f"expected {n} [N={N}, H_v={H_v}]; got {tuple(t.shape)}")
+    for t, n in ((A_log, "A_log"), (dt_bias, "dt_bias")):
+        if tuple(t.shape) != (H_v,):
+            raise ValueError(f"expected {n} [H_v={H_v}]; got {tuple(t.shape)}")
+    if z is not None and tuple(z.shape) != tuple(v.shape):
+        raise ValueError(f"expected z {tuple(v.shape)} (the shape of v); got {tuple(z.shape)}")
+    if norm_w is not None and tuple(norm_w.shape) != (V,):
+        raise ValueError(f"expected norm_w [V={V}]; got {tuple(norm_w.shape)}")
+    if out is not None and tuple(out.shape) != tuple(v.shape):
+        raise ValueError(f"expected out {tuple(v.shape)} (the shape of v); got {tuple(out.shape)}")
+
+
 def make_dims(q, v, state_pool, state_indices, *, k=None, a=None, b=None, z=None, out=None,
               max_T=None, split=0) -> gdn_dims:
     N, H_k, K = q.shape
@@ -143,7 +168,7 @@ def make_dims(q, v, state_pool, state_indices, *, k=None, a=None, b=None, z=None
     d = gdn_dims()
     d.batch, d.num_tokens, d.H_k, d.H_v, d.K, d.V = batch, N, H_k, H_v, K, V
     d.spec_stride = stride
-    d.max_T = stride if max_T is None else max_T
+    d.max_T = min(stride, 8) if max_T is None else max_T
     d.num_slots = state_pool.shape[0]
     d.q_stride = _row_stride(q, "q", H_k * K)
     d.k_stride = _row_stride(k, "k", H_k * K) if k is not None else 0
@@ -216,6 +241,7 @@ class PreparedCall:
 def prepare(q, k, v, a, b, z, A_log, dt_bias, norm_w, state_pool, state_indices, num_accepted,
             cu_seqlens, out, *, spec_token_indx=None, scale=128 ** -0.5, eps=1e-5, max_T=None,
             split=0, status=None) -> PreparedCall:
+    check_shapes(q, k, v, a, b, z, A_log, dt_bias, norm_w, out)
     dev = q.device
     if dev.type != "cuda":
         raise ValueError("gdn_spec_decode runs on CUDA tensors only")
@@ -292,6 +318,7 @@ def gdn_prefill_chunked(q, k, v, a, b, z, A_log, dt_bias, norm_w, state_pool, re
 
 def _prefill(entry, q, k, v, a, b, z, A_log, dt_bias, norm_w, state_pool, read_slots, write_slots,
              cu_seqlens, out, scale, eps, status, stream):
+    check_shapes(q, k, v, a, b, z, A_log, dt_bias, norm_w, out)
     dev = q.device
     if dev.type != "cuda":
         raise ValueError(f"{entry} runs on CUDA tensors only")
@@ -341,6 +368,17 @@ def gdn_spec_decode_conv(x, conv_weight, conv_bias, conv_pool, conv_in, conv_out
     None, conv_pool [num_conv_slots, state_len, conv_dim] bf16 (updated in
     place), conv_in / conv_out [B] int32; the other tensors as for
     gdn_spec_decode.  Returns ``out``."""
+    if x.dim() != 2 or state_pool.dim() != 4:
+        raise ValueError("expected x [N, conv_dim] and state_pool [num_slots, H_v, K, V]")
+    N, H_v, V = x.shape[0], state_pool.shape[1], state_pool.shape[3]
+    for t, n, shape in ((a, "a", (N, H_v)), (b, "b", (N, H_v)), (A_log, "A_log", (H_v,)),
+                        (dt_bias, "dt_bias", (H_v,)), (out, "out", (N, H_v, V))):
+        if tuple(t.shape) != shape:
+            raise ValueError(f"expected {n} {shape}; got {tuple(t.shape)}")
+    if z is not None and tuple(z.shape) != (N, H_v, V):
+        raise ValueError(f"expected z {(N, H_v, V)}; got {tuple(z.shape)}")
+    if norm_w is not None and tuple(norm_w.shape) != (V,):
+        raise ValueError(f"expected norm_w [V={V}]; got {tuple(norm_w.shape)}")
     dev = x.device
     if dev.type != "cuda":
         raise ValueError("gdn_spec_decode_conv runs on CUDA tensors only")
@@ -379,7 +417,7 @@ def gdn_spec_decode_conv(x, conv_weight, conv_bias, conv_pool, conv_in, conv_out
     d = gdn_dims()
     d.batch, d.num_tokens, d.H_k, d.H_v, d.K, d.V = state_indices.shape[0], N, H_k, H_v, K, V
     d.spec_stride = state_indices.shape[1]
-    d.max_T = d.spec_stride if max_T is None else max_T
+    d.max_T = min(d.spec_stride, 8) if max_T is None else max_T
     d.num_slots = state_pool.shape[0]
     d.a_stride = _row_stride(a, "a", H_v)
     d.b_stride = _row_stride(b, "b", H_v)

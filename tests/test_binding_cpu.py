@@ -33,6 +33,9 @@ def test_dense_dims():
 def test_max_T_defaults_to_the_slot_columns():
     t = _tensors(S=5)
     assert binding.make_dims(t["q"], t["v"], t["pool"], t["idx"]).max_T == 5
+    # a slot table wider than the 8-token limit: the default stays at 8
+    t = _tensors(S=12)
+    assert binding.make_dims(t["q"], t["v"], t["pool"], t["idx"]).max_T == 8
 
 
 def test_packed_mixed_qkv_views_carry_the_packed_row_stride():
@@ -72,3 +75,51 @@ def test_prepare_refuses_host_tensors_before_any_library_call():
     with pytest.raises(ValueError, match="CUDA"):
         binding.prepare(t["q"], t["k"], t["v"], t["a"], t["b"], t["z"], f32, t["a"][0], torch.zeros(K),
                         t["pool"], t["idx"], i32[:2], i32, t["out"])
+
+
+def _params():
+    return dict(A_log=torch.zeros(H_V, dtype=torch.float32), dt_bias=torch.zeros(H_V, dtype=torch.bfloat16),
+                norm_w=torch.zeros(K, dtype=torch.bfloat16))
+
+
+BAD_SHAPES = {
+    "a": lambda t, p: t.update(a=torch.zeros(5, H_V // 2, dtype=torch.bfloat16)),
+    "b": lambda t, p: t.update(b=torch.zeros(4, H_V, dtype=torch.bfloat16)),
+    "z": lambda t, p: t.update(z=torch.zeros(5, H_V // 2, K, dtype=torch.bfloat16)),
+    "out": lambda t, p: t.update(out=torch.zeros(4, H_V, K, dtype=torch.bfloat16)),
+    "dt_bias": lambda t, p: p.update(dt_bias=torch.zeros(H_V - 1, dtype=torch.bfloat16)),
+    "A_log": lambda t, p: p.update(A_log=torch.zeros(H_V // 2, dtype=torch.float32)),
+    "norm_w": lambda t, p: p.update(norm_w=torch.zeros(K // 2, dtype=torch.bfloat16)),
+    "v": lambda t, p: t.update(v=torch.zeros(6, H_V, K, dtype=torch.bfloat16)),
+}
+
+
+@pytest.mark.parametrize("field", sorted(BAD_SHAPES))
+def test_mismatched_sizes_are_refused_before_the_library(field, monkeypatch):
+    """A short a / b / z / out / dt_bias / A_log / norm_w (or a v with the wrong
+    token count) is refused by every entry point before the library is loaded
+    or called: the kernels would read or write past the end of such buffers."""
+    def no_library():
+        raise AssertionError("the library was reached")
+    monkeypatch.setattr(binding, "load_library", no_library)
+    t, p = _tensors(), _params()
+    BAD_SHAPES[field](t, p)
+    i32 = torch.zeros(3, dtype=torch.int32)
+    with pytest.raises(ValueError, match="expected"):
+        binding.prepare(t["q"], t["k"], t["v"], t["a"], t["b"], t["z"], p["A_log"], p["dt_bias"], p["norm_w"],
+                        t["pool"], t["idx"], i32[:2], i32, t["out"])
+    with pytest.raises(ValueError, match="expected"):
+        binding.gdn_prefill(t["q"], t["k"], t["v"], t["a"], t["b"], t["z"], p["A_log"], p["dt_bias"],
+                            p["norm_w"], t["pool"], i32[:2], i32[:2], i32, t["out"])
+    with pytest.raises(ValueError, match="expected"):
+        binding.gdn_prefill_chunked(t["q"], t["k"], t["v"], t["a"], t["b"], t["z"], p["A_log"], p["dt_bias"],
+                                    p["norm_w"], t["pool"], i32[:2], i32[:2], i32, t["out"])
+    if field != "v":
+        D = 2 * H_K * K + H_V * K
+        x = torch.zeros(5, D, dtype=torch.bfloat16)
+        w = torch.zeros(D, 4, dtype=torch.bfloat16)
+        cpool = torch.zeros(4, 6, D, dtype=torch.bfloat16)
+        with pytest.raises(ValueError, match="expected"):
+            binding.gdn_spec_decode_conv(x, w, None, cpool, i32[:2], i32[:2], t["a"], t["b"], t["z"],
+                                         p["A_log"], p["dt_bias"], p["norm_w"], t["pool"], t["idx"], i32[:2],
+                                         i32, t["out"], H_k=H_K)
