@@ -23,6 +23,8 @@ GDN_FLAG_QLEN = 4
 GDN_FLAG_TOKEN_ROW = 8
 GDN_FLAG_TIMEOUT = 16
 GDN_SPLIT_NARROW = 0x100     # dims.split flag: 8 V columns per warp (small batches)
+GDN_PRE_INDEX = 0x1          # dims.flags: the index tables were not written by the preceding kernel
+GDN_PRE_TOKENS = 0x2         # dims.flags (with GDN_PRE_INDEX): nor were the token inputs
 
 
 class gdn_dims(ctypes.Structure):
@@ -37,7 +39,7 @@ class gdn_dims(ctypes.Structure):
         ("q_stride", ctypes.c_int64), ("k_stride", ctypes.c_int64), ("v_stride", ctypes.c_int64),
         ("a_stride", ctypes.c_int64), ("b_stride", ctypes.c_int64), ("z_stride", ctypes.c_int64),
         ("out_stride", ctypes.c_int64),
-        ("split", ctypes.c_int32), ("reserved", ctypes.c_int32),
+        ("split", ctypes.c_int32), ("flags", ctypes.c_int32),
     ]
 
 
@@ -161,7 +163,7 @@ def check_shapes(q, k, v, a, b, z, A_log, dt_bias, norm_w, out=None):
 
 
 def make_dims(q, v, state_pool, state_indices, *, k=None, a=None, b=None, z=None, out=None,
-              max_T=None, split=0) -> gdn_dims:
+              max_T=None, split=0, flags=0) -> gdn_dims:
     N, H_k, K = q.shape
     H_v, V = v.shape[1], v.shape[2]
     batch, stride = state_indices.shape
@@ -178,23 +180,25 @@ def make_dims(q, v, state_pool, state_indices, *, k=None, a=None, b=None, z=None
     d.z_stride = _row_stride(z, "z", H_v * V) if z is not None else 0
     d.out_stride = _row_stride(out, "out", H_v * V) if out is not None else 0
     d.split = split
+    d.flags = flags
     return d
 
 
 def gdn_spec_decode(q, k, v, a, b, z, A_log, dt_bias, norm_w, state_pool, state_indices,
                     num_accepted, cu_seqlens, out, *, spec_token_indx=None, scale=128 ** -0.5,
-                    eps=1e-5, max_T=None, split=0, status=None, stream=None):
+                    eps=1e-5, max_T=None, split=0, flags=0, status=None, stream=None):
     """One speculative decode step (see include/gdnspec.h).  Tensors are CUDA
     tensors on one device: q, k [N, H_k, 128], v, z, out [N, H_v, 128], a, b
     [N, H_v], dt_bias [H_v], norm_w [128] in bf16; A_log [H_v] fp32;
     state_pool [num_slots, H_v, 128, 128] fp32 / bf16 / fp16 (updated in
     place); state_indices [B, spec_stride], num_accepted [B], cu_seqlens
     [B+1], spec_token_indx [sum q_len] (optional) and status [1] (optional)
-    int32.  Launches on ``stream`` (default: the current stream) and returns
-    ``out``."""
+    int32.  ``flags``: GDN_PRE_INDEX [| GDN_PRE_TOKENS] when those inputs were
+    not written by the kernel launched just before on the stream.  Launches on
+    ``stream`` (default: the current stream) and returns ``out``."""
     call = prepare(q, k, v, a, b, z, A_log, dt_bias, norm_w, state_pool, state_indices,
                    num_accepted, cu_seqlens, out, spec_token_indx=spec_token_indx, scale=scale,
-                   eps=eps, max_T=max_T, split=split, status=status)
+                   eps=eps, max_T=max_T, split=split, flags=flags, status=status)
     call(stream)
     return out
 
@@ -240,7 +244,7 @@ class PreparedCall:
 
 def prepare(q, k, v, a, b, z, A_log, dt_bias, norm_w, state_pool, state_indices, num_accepted,
             cu_seqlens, out, *, spec_token_indx=None, scale=128 ** -0.5, eps=1e-5, max_T=None,
-            split=0, status=None) -> PreparedCall:
+            split=0, flags=0, status=None) -> PreparedCall:
     check_shapes(q, k, v, a, b, z, A_log, dt_bias, norm_w, out)
     dev = q.device
     if dev.type != "cuda":
@@ -280,7 +284,8 @@ def prepare(q, k, v, a, b, z, A_log, dt_bias, norm_w, state_pool, state_indices,
     if state_pool.dim() != 4 or state_pool.shape[1] != v.shape[1] or state_pool.shape[2] != q.shape[2] or \
             state_pool.shape[3] != v.shape[2]:
         raise ValueError("expected state_pool [num_slots, H_v, K, V]")
-    dims = make_dims(q, v, state_pool, state_indices, k=k, a=a, b=b, z=z, out=out, max_T=max_T, split=split)
+    dims = make_dims(q, v, state_pool, state_indices, k=k, a=a, b=b, z=z, out=out, max_T=max_T, split=split,
+                     flags=flags)
     args = [_ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(b), _ptr(z), _ptr(A_log), _ptr(dt_bias), _ptr(norm_w),
             _ptr(state_pool), _ptr(state_indices), _ptr(num_accepted), _ptr(cu_seqlens),
             _ptr(spec_token_indx), _ptr(out)]
@@ -360,7 +365,7 @@ def _prefill(entry, q, k, v, a, b, z, A_log, dt_bias, norm_w, state_pool, read_s
 
 def gdn_spec_decode_conv(x, conv_weight, conv_bias, conv_pool, conv_in, conv_out, a, b, z, A_log, dt_bias,
                          norm_w, state_pool, state_indices, num_accepted, cu_seqlens, out, *, H_k, K=128,
-                         spec_token_indx=None, scale=128 ** -0.5, eps=1e-5, max_T=None, status=None,
+                         spec_token_indx=None, scale=128 ** -0.5, eps=1e-5, max_T=None, flags=0, status=None,
                          stream=None):
     """The speculative step with the short causal convolution fused in front
     (see include/gdnspec.h): x [N, conv_dim] bf16 projection rows (channels
@@ -423,6 +428,7 @@ def gdn_spec_decode_conv(x, conv_weight, conv_bias, conv_pool, conv_in, conv_out
     d.b_stride = _row_stride(b, "b", H_v)
     d.z_stride = _row_stride(z, "z", H_v * V) if z is not None else 0
     d.out_stride = _row_stride(out, "out", H_v * V)
+    d.flags = flags
     cd = gdn_conv_dims()
     cd.width = conv_weight.shape[1]
     cd.state_len = conv_pool.shape[1]

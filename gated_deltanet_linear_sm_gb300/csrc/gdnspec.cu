@@ -614,12 +614,26 @@ gdn_spec_decode_kernel(const __grid_constant__ Params p) {
 
     // Launched with programmatic stream serialization: this CTA may become
     // resident while the previous kernel in the stream is still running.  It
-    // waits here, before its first global access, until that grid has
-    // completed and its writes are visible; and it lets the next kernel's
-    // CTAs be scheduled as soon as every CTA of this grid has started.  Only
-    // the launch latency between back-to-back steps is hidden.
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // waits (dep_wait) until that grid has completed and its writes are
+    // visible before it touches memory the grid may have written, then lets
+    // the next kernel's CTAs be scheduled.  By default the wait comes before
+    // the first global access; GDN_PRE_INDEX moves it after the index reads,
+    // GDN_PRE_TOKENS (with it) after the token prologue as well, so that those
+    // reads overlap the previous grid's tail.  The state tile, out, the conv
+    // slots and the status word are touched only after the wait; every exit
+    // waits first, so that no successor is released before this grid's
+    // predecessor has completed.
+    const bool pre_index = (p.flags & GDN_PRE_INDEX) != 0;
+    const bool pre_tokens = !CONV && pre_index && (p.flags & GDN_PRE_TOKENS) != 0;
+    bool waited = false;
+    auto dep_wait = [&]() {
+        if (!waited) {
+            asm volatile("griddepcontrol.wait;" ::: "memory");
+            asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+            waited = true;
+        }
+    };
+    if (!pre_index) dep_wait();
 
     // ---- resolve the work item (every thread computes the same answer) ----
     // The sequence's slot row is read in the same round trip as its length and
@@ -638,12 +652,12 @@ gdn_spec_decode_kernel(const __grid_constant__ Params p) {
         conv_in = __ldg(p.conv_in + i);
         conv_out = __ldg(p.conv_out + i);
     }
-    if (q_len <= 0) return;                                    // nothing to do
+    if (q_len <= 0) { dep_wait(); return; }                    // nothing to do
     // token positions must lie inside [0, cu_seqlens[batch]), the length of
     // spec_token_indx (rows themselves are range-checked below)
-    if (bos < 0 || bos + q_len > cu_total) { raise_flag(p, rank, GDN_FLAG_TOKEN_ROW); return; }
-    if (acc > p.stride) { raise_flag(p, rank, GDN_FLAG_ACCEPTED); return; }
-    if (q_len > p.max_T || q_len > p.stride) { raise_flag(p, rank, GDN_FLAG_QLEN); return; }
+    if (bos < 0 || bos + q_len > cu_total) { dep_wait(); raise_flag(p, rank, GDN_FLAG_TOKEN_ROW); return; }
+    if (acc > p.stride) { dep_wait(); raise_flag(p, rank, GDN_FLAG_ACCEPTED); return; }
+    if (q_len > p.max_T || q_len > p.stride) { dep_wait(); raise_flag(p, rank, GDN_FLAG_QLEN); return; }
     // rewind: the state after the last accepted token; acc-1 clamped at 0
     const int rj = max(acc - 1, 0);
     long long rs = 0;
@@ -651,22 +665,27 @@ gdn_spec_decode_kernel(const __grid_constant__ Params p) {
     for (int j = 0; j < kMaxT; ++j)
         if (j == rj) rs = slots[j];
     if (rj >= kMaxT) rs = __ldg(slot_row + rj);                // acceptance beyond the first 8 columns
-    if (rs < 0) return;                                        // padded sequence
-    if (rs >= p.num_slots) { raise_flag(p, rank, GDN_FLAG_SLOT_RANGE); return; }
+    if (rs < 0) { dep_wait(); return; }                        // padded sequence
+    if (rs >= p.num_slots) { dep_wait(); raise_flag(p, rank, GDN_FLAG_SLOT_RANGE); return; }
     if constexpr (CONV) {
         if (conv_in >= p.num_conv_slots || conv_out >= p.num_conv_slots) {
+            dep_wait();
             raise_flag(p, rank, GDN_FLAG_SLOT_RANGE);
             return;
         }
     }
+    if (!pre_tokens) dep_wait();
 
     // ---- load this lane's R x 4 block of the state tile (FP32 in registers):
-    //      rows rg + G r, columns col0 .. col0 + 3 ----
+    //      rows rg + G r, columns col0 .. col0 + 3; issued before the token
+    //      prologue, or after it when the prologue runs ahead of the wait ----
     const StateT* src = static_cast<const StateT*>(p.pool) + (rs * p.H_v + h) * kTile;
     float S[L::kRows][4];
+    if (!pre_tokens) {
 #pragma unroll
-    for (int r = 0; r < L::kRows; ++r)
-        StateIO<StateT>::load4(src + static_cast<int64_t>(rg + L::kRowGroups * r) * kV + col0, S[r]);
+        for (int r = 0; r < L::kRows; ++r)
+            StateIO<StateT>::load4(src + static_cast<int64_t>(rg + L::kRowGroups * r) * kV + col0, S[r]);
+    }
 
     // ---- per-token prologue: gather rows, gates, normalised q / k, v, z ----
     const int kh = h / p.group;
@@ -702,6 +721,12 @@ gdn_spec_decode_kernel(const __grid_constant__ Params p) {
                 }
             }
         }
+    }
+    if (pre_tokens) {
+        dep_wait();
+#pragma unroll
+        for (int r = 0; r < L::kRows; ++r)
+            StateIO<StateT>::load4(src + static_cast<int64_t>(rg + L::kRowGroups * r) * kV + col0, S[r]);
     }
     // publishes the prologue; every CTA of the cluster checks every token row,
     // so the skip decision below is the same in all of them
@@ -941,7 +966,7 @@ int choose_split(int64_t units, gdn_dtype dt) {
 gdn_status check_dims(const gdn_dims* d) {
     if (d == nullptr) return GDN_ERR_NULL_ARG;
     if (d->batch < 0 || d->num_tokens < 0 || d->H_k <= 0 || d->H_v <= 0 || d->spec_stride < 1 ||
-        d->num_slots < 1 || d->H_v % d->H_k != 0 || d->reserved != 0)
+        d->num_slots < 1 || d->H_v % d->H_k != 0 || (d->flags & ~(GDN_PRE_INDEX | GDN_PRE_TOKENS)) != 0)
         return GDN_ERR_BAD_SHAPE;
     if (d->max_T < 1 || d->max_T > kMaxT) return GDN_ERR_BAD_SHAPE;
     if (d->q_stride < 0 || d->k_stride < 0 || d->v_stride < 0 || d->a_stride < 0 || d->b_stride < 0 ||
@@ -959,7 +984,7 @@ gdn_status check_dims(const gdn_dims* d) {
 gdn_status check_common_dims(const gdn_dims* d) {
     if (d == nullptr) return GDN_ERR_NULL_ARG;
     if (d->batch < 0 || d->num_tokens < 0 || d->H_k <= 0 || d->H_v <= 0 || d->num_slots < 1 ||
-        d->H_v % d->H_k != 0 || d->reserved != 0)
+        d->H_v % d->H_k != 0 || d->flags != 0)
         return GDN_ERR_BAD_SHAPE;
     if (d->q_stride < 0 || d->k_stride < 0 || d->v_stride < 0 || d->a_stride < 0 || d->b_stride < 0 ||
         d->z_stride < 0 || d->out_stride < 0)
@@ -1008,6 +1033,7 @@ gdn_status make_params(Params& p, const void* q, const void* k, const void* v, c
     p.stride = dims->spec_stride;
     p.max_T = dims->max_T;
     p.group = dims->H_v / dims->H_k;
+    p.flags = dims->flags;
     p.scale = scale;
     p.eps = eps;
     // vector accesses: 16 B state rows, 8 B bf16 quads
@@ -1096,7 +1122,7 @@ gdn_status gdn_spec_decode_conv(const void* x, const void* conv_weight, const vo
         static_cast<int64_t>(cdims->state_len) < cdims->width - 1 + static_cast<int64_t>(dims->spec_stride))
         return GDN_ERR_BAD_SHAPE;
     if (state_dtype != GDN_F32 && state_dtype != GDN_BF16 && state_dtype != GDN_F16) return GDN_ERR_UNSUPPORTED;
-    if (dims->split > 1) return GDN_ERR_UNSUPPORTED;
+    if (dims->split > 1 || (dims->flags & GDN_PRE_TOKENS)) return GDN_ERR_UNSUPPORTED;
     if (dims->batch == 0) return GDN_OK;
     if (!state_indices || !num_accepted || !x || !conv_weight || !conv_pool || !conv_in || !conv_out)
         return GDN_ERR_NULL_ARG;

@@ -48,8 +48,9 @@
 extern "C" {
 #endif
 
-/* 2: gdn_spec_decode_split takes the state dtype; dims->split accepts GDN_SPLIT_NARROW */
-#define GDNSPEC_VERSION 2
+/* 2: gdn_spec_decode_split takes the state dtype; dims->split accepts GDN_SPLIT_NARROW
+   3: dims->flags (formerly reserved): GDN_PRE_INDEX, GDN_PRE_TOKENS */
+#define GDNSPEC_VERSION 3
 
 #if defined(__GNUC__)
 #define GDNSPEC_API __attribute__((visibility("default")))
@@ -92,6 +93,32 @@ typedef enum { GDN_F32 = 0, GDN_BF16 = 1, GDN_F16 = 2 } gdn_dtype;
  */
 #define GDN_SPLIT_NARROW 0x100
 
+/*
+ * dims->flags: what the caller promises about the kernel launched on the
+ * stream immediately before this call.  Each decode launch lets the next
+ * launch on the stream start its CTAs while it finishes (programmatic
+ * dependent launch); a CTA then waits for its predecessor to complete before
+ * it touches memory that the predecessor may have written.  With these flags
+ * it reads some inputs before that wait, which hides their latency behind the
+ * predecessor's tail:
+ *   GDN_PRE_INDEX   state_indices, num_accepted, cu_seqlens and
+ *                   spec_token_indx were not written by the preceding kernel
+ *                   (for example: they were filled at the start of the step);
+ *   GDN_PRE_TOKENS  with GDN_PRE_INDEX: neither were q, k, v, a, b, z, A_log,
+ *                   dt_bias and norm_w (for example: the batch's inputs are
+ *                   resident and the preceding kernel is another decode step).
+ * The state pool, out and status_word are always accessed after the wait, so
+ * back-to-back steps that rewind into each other's slots stay ordered.  A
+ * decode launch signals its successor only after its own wait, so when the
+ * preceding kernel is one of this library's decode launches, or a kernel that
+ * does not use programmatic dependent launch, every kernel before it has
+ * completed when the early reads happen.
+ * gdn_spec_decode_conv accepts GDN_PRE_INDEX only; the prefill entry points
+ * take no flags.
+ */
+#define GDN_PRE_INDEX  0x1
+#define GDN_PRE_TOKENS 0x2
+
 /* Opaque CUDA stream handle; the same type as cudaStream_t (NULL = legacy default stream). */
 typedef struct CUstream_st* gdn_stream_t;
 
@@ -115,7 +142,7 @@ typedef struct {
                              (each warp owns 16 V columns), or GDN_SPLIT_NARROW
                              | 2 or | 4 (each warp owns 8 V columns: 16 warps
                              per unit over 2 or 4 CTAs) */
-    int32_t reserved;     /* must be 0 */
+    int32_t flags;        /* 0, or GDN_PRE_INDEX [| GDN_PRE_TOKENS] (above); 0 for the prefill entry points */
 } gdn_dims;
 
 /*

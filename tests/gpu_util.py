@@ -66,7 +66,7 @@ def make_pool(case, device, seed=1234, slots=None):
     return pool
 
 
-def run_gpu(case, device, pool=None, *, split=0, out=None, status=True, tensors=None, stream=None):
+def run_gpu(case, device, pool=None, *, split=0, flags=0, out=None, status=True, tensors=None, stream=None):
     """Run the CUDA path; returns (out, pool, status_word)."""
     t = tensors if tensors is not None else device_tensors(case, device)
     if pool is None:
@@ -78,7 +78,7 @@ def run_gpu(case, device, pool=None, *, split=0, out=None, status=True, tensors=
     gdn.gdn_spec_decode(t["q"], t["k"], t["v"], t["a"], t["b"], t["z"], t["A_log"], t["dt_bias"],
                         t["norm_w"], pool, t["state_indices"], t["num_accepted"], t["cu_seqlens"], out,
                         spec_token_indx=t["spec_token_indx"], scale=case.scale, eps=case.eps,
-                        max_T=case.max_T, split=split, status=st, stream=stream)
+                        max_T=case.max_T, split=split, flags=flags, status=st, stream=stream)
     return out, pool, st
 
 

@@ -25,7 +25,7 @@ def test_dense_dims():
     d = binding.make_dims(t["q"], t["v"], t["pool"], t["idx"], k=t["k"], a=t["a"], b=t["b"], z=t["z"],
                           out=t["out"], max_T=2, split=0)
     assert (d.batch, d.num_tokens, d.H_k, d.H_v, d.K, d.V) == (2, 5, H_K, H_V, K, K)
-    assert (d.spec_stride, d.max_T, d.num_slots, d.split, d.reserved) == (3, 2, 8, 0, 0)
+    assert (d.spec_stride, d.max_T, d.num_slots, d.split, d.flags) == (3, 2, 8, 0, 0)
     assert (d.q_stride, d.k_stride, d.v_stride) == (H_K * K, H_K * K, H_V * K)
     assert (d.a_stride, d.b_stride, d.z_stride, d.out_stride) == (H_V, H_V, H_V * K, H_V * K)
 

@@ -97,7 +97,7 @@ def _call(lib, dims, *, ptr=0x1000, z=0x1000, w=0x1000, state_dtype=0):
     (dict(K=64), 3), (dict(V=256), 3), (dict(H_v=12, H_k=8), 2), (dict(max_T=9), 2),
     (dict(max_T=0), 2), (dict(spec_stride=0), 2), (dict(batch=-1), 2), (dict(num_slots=0), 2),
     (dict(split=3), 3), (dict(split=0x101), 3), (dict(split=0x108), 3), (dict(split=0x100), 3),
-    (dict(reserved=1), 2), (dict(q_stride=-4), 2),
+    (dict(flags=4), 2), (dict(flags=-1), 2), (dict(q_stride=-4), 2),
 ])
 def test_bad_dims_rejected(lib, over, code):
     assert _call(lib, _dims(**over)) == code
@@ -164,6 +164,8 @@ def test_conv_bad_pointers_rejected(lib):
     assert _call_conv(lib, _dims(), _cdims(), bias=0x1002) == 4   # bias not 8-byte aligned
     assert _call_conv(lib, _dims(split=2), _cdims()) == 3         # the fused path has no split
     assert _call_conv(lib, _dims(split=binding.GDN_SPLIT_NARROW | 2), _cdims()) == 3
+    # the conv history may be the preceding step's output: token inputs are never read early
+    assert _call_conv(lib, _dims(flags=binding.GDN_PRE_INDEX | binding.GDN_PRE_TOKENS), _cdims()) == 3
     assert _call_conv(lib, _dims(batch=0), _cdims(), ptr=0) == 0  # empty batch: nothing launched
     assert lib.gdn_spec_decode_conv(*([None] * 6), None, *([None] * 12), ctypes.byref(_dims()), 0.1, 1e-5, 0,
                                     None, None) == 1
@@ -175,3 +177,13 @@ def test_pool_beyond_32bit_rows_is_unsupported(lib):
     anything touches the GPU)."""
     assert _call(lib, _dims(num_slots=(1 << 31) // (8 * 128))) == 3
     assert _call_conv(lib, _dims(num_slots=(1 << 31) // (8 * 128)), _cdims()) == 3
+
+
+def test_prefill_entry_points_take_no_flags(lib):
+    """The early-read flags are a decode-step feature; the prefill entry points
+    reject any flag before launching anything."""
+    P = 0x1000
+    for name in ("gdn_prefill", "gdn_prefill_chunked"):
+        fn = getattr(lib, name)
+        assert fn(P, P, P, P, P, P, P, P, P, P, P, P, P, P, ctypes.byref(_dims(flags=1)), 0.088, 1e-5, 0,
+                  None, None) == 2

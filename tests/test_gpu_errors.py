@@ -28,14 +28,14 @@ def _rows_of(case, i):
     return case.token_rows()[case.cu_seqlens[i]:case.cu_seqlens[i + 1]]
 
 
-def _run_and_check(case, gpu_case, flag, skipped_seq=True, expect=None, split=0):
+def _run_and_check(case, gpu_case, flag, skipped_seq=True, expect=None, split=0, flags=0):
     """Run gpu_case (the corrupted one); compare every other sequence with the
     oracle on `expect` (default: case), check the flag and that the corrupted
     sequence left its slots and rows alone."""
     dev = torch.device("cuda", 0)
     pool = make_pool(case, dev)
     before = pool.clone()
-    out, pool, st = run_gpu(gpu_case, dev, pool, split=split)
+    out, pool, st = run_gpu(gpu_case, dev, pool, split=split, flags=flags)
     torch.cuda.synchronize()
     assert int(st.item()) & flag, int(st.item())
     good = [i for i in range(case.batch) if not (skipped_seq and i == BAD)]
@@ -54,6 +54,19 @@ def test_num_accepted_beyond_stride(split):
     bad = dataclasses.replace(case, num_accepted=case.num_accepted.copy())
     bad.num_accepted[BAD] = case.spec_stride + 1
     _run_and_check(case, bad, gdn.binding.GDN_FLAG_ACCEPTED, split=split)
+
+
+@pytest.mark.parametrize("flags", [1, 3])
+def test_bad_data_with_early_reads(flags):
+    """The exits taken on bad index data come before the dependency wait when
+    the index tables are read early; each still waits before it reports."""
+    case = _base()
+    bad = dataclasses.replace(case, num_accepted=case.num_accepted.copy(), state_indices=case.state_indices.copy())
+    bad.num_accepted[BAD] = case.spec_stride + 1
+    _run_and_check(case, bad, gdn.binding.GDN_FLAG_ACCEPTED, flags=flags)
+    bad = dataclasses.replace(case, state_indices=case.state_indices.copy())
+    bad.state_indices[BAD, max(int(case.num_accepted[BAD]) - 1, 0)] = case.num_slots + 7
+    _run_and_check(case, bad, gdn.binding.GDN_FLAG_SLOT_RANGE, flags=flags)
 
 
 @pytest.mark.parametrize("split", [1, 8, 0x102])

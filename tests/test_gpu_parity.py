@@ -14,8 +14,8 @@ import pytest
 import torch
 
 from gated_deltanet_linear_sm_gb300 import synth
-from tests.gpu_util import (OUT_SENTINEL, active_rows, compare, make_pool, run_gpu, to_host_bits,
-                            written_slots)
+from tests.gpu_util import (OUT_SENTINEL, active_rows, compare, device_tensors, make_pool, run_gpu,
+                            to_host_bits, written_slots)
 from tests.util import bf16_bits, bf16_values
 
 pytestmark = pytest.mark.gpu
@@ -160,9 +160,11 @@ def test_ordinary_decode_identity(cuda_device):
     assert np.all(np.abs(gs - ws) <= 3e-2 + 3e-2 * np.abs(ws))
 
 
-def test_two_steps_chain(cuda_device):
+@pytest.mark.parametrize("flags", [0, 1, 3])
+def test_two_steps_chain(cuda_device, flags):
     """Step 2 reads the slots step 1 wrote: two GPU calls in a row equal two
-    oracle calls in a row."""
+    oracle calls in a row (also with the index tables and token rows read
+    before the dependency wait: the state still waits for step 1)."""
     from oracle import oracle as orc
     from tests.util import bf16_values, initial_pool
     case1 = synth.make_case(batch=8, H_k=1, H_v=8, T=4, state_dtype=synth.F32, num_slots=96, seed=27)
@@ -178,9 +180,10 @@ def test_two_steps_chain(cuda_device):
     case2.state_indices = idx2
     pool = make_pool(case1, cuda_device)
     hp = initial_pool(case1)
-    out1, pool, _ = run_gpu(case1, cuda_device, pool)
+    t2 = device_tensors(case2, cuda_device)               # step 2's inputs resident before step 1 runs
+    out1, pool, _ = run_gpu(case1, cuda_device, pool, flags=flags)
     r1 = orc.run_case(case1, hp)
-    out2, pool, _ = run_gpu(case2, cuda_device, pool)
+    out2, pool, _ = run_gpu(case2, cuda_device, pool, flags=flags, tensors=t2)
     r2 = orc.run_case(case2, hp)
     torch.cuda.synchronize()
     for out, r in ((out1, r1), (out2, r2)):
@@ -214,7 +217,8 @@ def test_packed_mixed_qkv_strides(cuda_device):
     compare(case, out, pool)
 
 
-def test_graph_capture_replays(cuda_device):
+@pytest.mark.parametrize("flags", [0, 3])
+def test_graph_capture_replays(cuda_device, flags):
     """A call captured in a CUDA graph and replayed gives the same bits as an
     eager call on the same inputs (the launch needs no host sync)."""
     import gated_deltanet_linear_sm_gb300 as gdn
@@ -227,7 +231,8 @@ def test_graph_capture_replays(cuda_device):
         pool = pool0.clone()
         out = torch.zeros(case.num_tokens, case.H_v, case.V, dtype=torch.bfloat16, device=cuda_device)
         call = gdn.prepare(t["q"], t["k"], t["v"], t["a"], t["b"], t["z"], t["A_log"], t["dt_bias"],
-                           t["norm_w"], pool, t["state_indices"], t["num_accepted"], t["cu_seqlens"], out)
+                           t["norm_w"], pool, t["state_indices"], t["num_accepted"], t["cu_seqlens"], out,
+                           flags=flags)
         if mode == "eager":
             call()
         else:
@@ -277,3 +282,24 @@ def test_gate_and_input_extremes(cuda_device, split):
                               k=bf16_bits(k), A_log=A_log.astype(np.float32), pool_std=30.0)
     m = _full_check(ext, cuda_device, split)
     assert m["out_rel_l2"] < 5e-4
+
+
+@pytest.mark.parametrize("split", [1, 2, 0x102])
+@pytest.mark.parametrize("sd", [synth.F32, synth.BF16])
+def test_early_read_flags_change_no_bit(cuda_device, sd, split):
+    """GDN_PRE_INDEX and GDN_PRE_INDEX | GDN_PRE_TOKENS move reads ahead of the
+    dependency wait; the results (out and every pool byte) are bit-identical to
+    flags = 0, on a ragged, padded batch."""
+    import gated_deltanet_linear_sm_gb300 as gdn
+    case = synth.make_case(batch=24, H_k=2, H_v=16, T=8, state_dtype=sd, num_slots=400, q_lens="ragged",
+                           pad_prob=0.1, seed=31)
+    pool0 = make_pool(case, cuda_device)
+    res = []
+    for flags in (0, gdn.binding.GDN_PRE_INDEX, gdn.binding.GDN_PRE_INDEX | gdn.binding.GDN_PRE_TOKENS):
+        out, pool, st = run_gpu(case, cuda_device, pool0.clone(), split=split, flags=flags)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        dt = torch.int32 if sd == synth.F32 else torch.int16
+        res.append((out.view(torch.int16).clone(), pool.view(dt).clone()))
+    for r in res[1:]:
+        assert torch.equal(r[0], res[0][0]) and torch.equal(r[1], res[0][1])
