@@ -315,8 +315,8 @@ def gdn_prefill(q, k, v, a, b, z, A_log, dt_bias, norm_w, state_pool, read_slots
 def gdn_prefill_chunked(q, k, v, a, b, z, A_log, dt_bias, norm_w, state_pool, read_slots, write_slots,
                         cu_seqlens, out, *, scale=128 ** -0.5, eps=1e-5, status=None, stream=None):
     """The same prefill as gdn_prefill, computed chunk by chunk on the tensor
-    cores (bf16 operands, FP32 accumulation; see include/gdnspec.h).  Same
-    arguments; returns ``out``."""
+    cores at FP32 accuracy (hi / lo bf16 operand parts, FP32 accumulation; see
+    include/gdnspec.h).  Same arguments; returns ``out``."""
     return _prefill("gdn_prefill_chunked", q, k, v, a, b, z, A_log, dt_bias, norm_w, state_pool, read_slots,
                     write_slots, cu_seqlens, out, scale, eps, status, stream)
 

@@ -17,22 +17,27 @@
 // are e^(non-positive), so nothing overflows however strong the decay.
 //
 // Kernel (one CTA of 8 warps per (sequence, v-head), one CTA per SM):
-//  * Products are 128-row tcgen05.mma (kind::f16: bf16 operands, FP32
-//    accumulators) issued by one thread.  Operands are 128-byte-swizzled
-//    K-major tiles in shared memory; accumulators live in tensor memory:
+//  * Products run on the tensor cores as 128-row tcgen05.mma (kind::f16: bf16
+//    operands, FP32 accumulators) issued by one thread, at FP32 accuracy: every
+//    operand x is carried as two bf16 terms, hi = bf16(x) and lo = bf16(x - hi)
+//    (|x - hi - lo| <= 2^-18 |x|), and a product accumulates the hi.hi, lo.hi
+//    and hi.lo terms in FP32 (the lo.lo term is below 2^-18).  A token operand
+//    (64 rows) stores hi and lo side by side along K, so the tensor cores add
+//    the terms inside the accumulator: its products land in lanes 0-63, and
+//    lanes 64-127 (the MMA's rows past the tile) are never read.  Operands are
+//    128-byte-swizzled K-major tiles in shared memory; accumulators live in
+//    tensor memory:
 //      columns   0- 63 P = K^ K^^T         columns  64-127 R = Q^ K^^T
 //      columns 128-255 X = K^ S            columns 256-383 O = Q^ S, then
 //                                          e^G O + R~ V' (the chunk's output)
 //      columns 384-511 S^T (FP32, carried over the whole prompt)
-//    Token-row operands hold the chunk in rows 0-63; rows 64-127 are zero
-//    and their results unused.
 //  * The FP32 state stays in tensor memory from the first chunk to the last.
 //    Per chunk it is rescaled by e^(G_last) (tcgen05.ld / st) and V'^T K~ is
-//    accumulated into it by one MMA.  Its bf16 image is the B operand of X
+//    accumulated into it; its hi and lo bf16 images are the B operands of X
 //    and O for the next chunk.
-//  * The unit lower-triangular solve runs on CUDA cores, two threads per
-//    value column with the column in registers, right-looking so that each
-//    step is a batch of independent FMAs.
+//  * The unit lower-triangular solve runs on CUDA cores in FP32, two threads
+//    per value column with the column in registers, right-looking so that
+//    each step is a batch of independent FMAs.
 //  * Every wait on the tensor cores is bounded.  On a timeout the CTA sets
 //    GDN_FLAG_TIMEOUT, waits (bounded) for the MMAs in flight, releases its
 //    tensor memory and stops.
@@ -62,23 +67,35 @@ constexpr uint32_t kSpinLimit = 1u << 24;       // try_wait polls before giving 
 // 128-byte-swizzled K-major bf16 tiles (the canonical SWIZZLE_128B layout):
 // a tile of R rows is stored in atom columns of 64 elements; element (r, c)
 // sits at (c / 64) * R * 128 + r * 128 + (((c % 64) / 8) ^ (r % 8)) * 16 + (c % 8) * 2.
-constexpr int kTileK = 0;                       // K^    [128 t ][128 kd]
-constexpr int kTileQ = kTileK + 32768;          // Q^    [128 t ][128 kd]
-constexpr int kTileS = kTileQ + 32768;          // S^T   [128 v ][128 kd]
-constexpr int kTileR = kTileS + 32768;          // R~    [128 t ][ 64 s ]
-constexpr int kTileV = kTileR + 16384;          // V'^T  [128 v ][ 64 t ]
-constexpr int kTileKd = kTileV + 16384;         // K~^T  [128 kd][ 64 t ]
+// Token tiles have 64 rows and carry hi in columns 0 .. K-1, lo in K .. 2K-1.
+// Regions are reused once the products that read them have completed:
+//   kTileK   [64 t][hi 128 | lo 128 kd]   K^        after phase 2: the FP32 gate w silu(z) [64 t][128 v]
+//   kTileQ   [64 t][hi 128 | lo 128 kd]   Q^        after MMA 1: K~^T hi | lo  [128 kd][64 t] each
+//   kTileS   [128 v][128 kd]              S^T hi
+//   kTileS2  [128 v][128 kd]              S^T lo    after MMA 1: V'^T hi | lo  [128 v][64 t] each
+//   kTileR   [64 t][hi 64 | lo 64 s]      R~
+// A 128-row MMA over a 64-row tile reads 8 KB past each atom column; every
+// such read stays inside the shared-memory block and lands in unread lanes.
+constexpr int kTileK = 0;
+constexpr int kTileQ = kTileK + 32768;
+constexpr int kTileS = kTileQ + 32768;
+constexpr int kTileS2 = kTileS + 32768;
+constexpr int kTileR = kTileS2 + 32768;
+constexpr int kTileKdHi = kTileQ, kTileKdLo = kTileQ + 16384;
+constexpr int kTileVHi = kTileS2, kTileVLo = kTileS2 + 16384;
+constexpr int kGate = kTileK;                   // FP32 [64 t][128 v], column v stored at v ^ (t % 32)
 constexpr int kA2Half = 36;                     // floats per parity half-row (32 used; the pad puts
                                                 // the two halves of a row on different banks)
 constexpr int kA2Row = 2 * kA2Half;
-constexpr int kA2 = kTileKd + 16384;            // A     fp32 [64 s][2 parity][36 (t/2)]
+constexpr int kA2 = kTileR + 16384;             // A     fp32 [64 s][2 parity][36 (t/2)]
 constexpr int kBStride = kC + 1;                // odd row pitch: column walks are conflict-free
 constexpr int kBT = kA2 + kC * kA2Row * 4;      // B^T   fp32 [128 v][65]
 constexpr int kStagePitch = kV / 4 + 1;         // uint2 per padded output-staging row (aliases B^T)
 static_assert(kC * kStagePitch * 8 <= kV * kBStride * 4, "staging fits the B^T region");
 constexpr int kZStride = kV / 4 + 1;            // uint2 per padded gate row
-constexpr int kZ = kBT + kV * kBStride * 4;     // w silu(z), bf16 quads [64 t][33]
+constexpr int kZ = kBT + kV * kBStride * 4;     // raw z, bf16 quads [64 t][33]
 constexpr int kMisc = kZ + kC * kZStride * 8;
+static_assert(kTileR + 16384 + 8192 <= kMisc, "the R~ tile's unread rows stay inside the block");
 
 struct Misc {
     unsigned long long bar;                     // MMA completion barrier
@@ -86,6 +103,7 @@ struct Misc {
     float gamma;                                // e^(G_last) of the current chunk
     float g[kC], G[kC], beta[kC], eG[kC], kfac[kC];   // G 16-byte aligned (float4 reads)
     float ssq[2][kC];                           // per-row sums of squares of the two column halves
+    float wn[kV];                               // norm_w
     int row[kC];
 };
 static_assert(kMisc % 16 == 0 && offsetof(Misc, G) % 16 == 0, "float4 reads of G");
@@ -104,9 +122,21 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<const uint32_t*>(&h);
 }
-__device__ __forceinline__ uint4 pack8(const float* x) {
-    return make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]), pack_bf16x2(x[4], x[5]),
-                      pack_bf16x2(x[6], x[7]));
+// (a, b) -> bf16 hi pair and the bf16 pair of the remainders x - hi (the
+// remainder of a round-to-nearest bf16 is exact in FP32)
+__device__ __forceinline__ void split2(float a, float b, uint32_t& hi, uint32_t& lo) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    const float2 hf = __bfloat1622float2(h);
+    const __nv_bfloat162 l = __floats2bfloat162_rn(a - hf.x, b - hf.y);
+    hi = *reinterpret_cast<const uint32_t*>(&h);
+    lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+// 8 values -> the 16-byte chunks of their hi and lo parts
+__device__ __forceinline__ void split8(const float* x, uint4& hi, uint4& lo) {
+    split2(x[0], x[1], hi.x, lo.x);
+    split2(x[2], x[3], hi.y, lo.y);
+    split2(x[4], x[5], hi.z, lo.z);
+    split2(x[6], x[7], hi.w, lo.w);
 }
 
 // ---- tcgen05 / mbarrier ---------------------------------------------------------------
@@ -145,6 +175,17 @@ __device__ __forceinline__ void gemm(uint32_t d, uint32_t a_tile, int a_rows, ui
         const uint32_t ob = (ks >> 2) * b_rows * 128 + (ks & 3) * 32;
         mma_bf16(d, desc_sw128(a_tile + oa), desc_sw128(b_tile + ob), idesc, (accumulate || ks > 0) ? 1u : 0u);
     }
+}
+
+// D[128][N] (+)= A B^T at FP32 accuracy from hi / lo parts: the hi.hi, lo.hi
+// and hi.lo terms over K.  a_hi / a_lo and b_hi / b_lo are the tiles (or the
+// column halves of one tile) holding the parts; a_rows / b_rows their row
+// counts (the stride between atom columns).
+__device__ __forceinline__ void gemm_split(uint32_t d, uint32_t a_hi, uint32_t a_lo, int a_rows, uint32_t b_hi,
+                                           uint32_t b_lo, int b_rows, int N, int K, bool accumulate) {
+    gemm(d, a_hi, a_rows, b_hi, b_rows, N, K, accumulate);
+    gemm(d, a_lo, a_rows, b_hi, b_rows, N, K, true);
+    gemm(d, a_hi, a_rows, b_lo, b_rows, N, K, true);
 }
 
 __device__ __forceinline__ void commit(uint32_t bar) {
@@ -265,25 +306,25 @@ __device__ __forceinline__ float silu(float z) { return __fdividef(z, 1.0f + __e
 // ---- the kernel -------------------------------------------------------------------------
 //
 // Per chunk, with the warps' TMEM quadrants q = warp % 4 (tcgen05.ld / st reach
-// only lanes 32q .. 32q + 31, so token rows 0-63 are reachable from warps 0, 1,
-// 4, 5 only):
-//   phase 1  all warps        k^, q^, v, z, gates of the chunk's 64 tokens; the
-//                             running sum G; K~^T
+// only lanes 32q .. 32q + 31: token rows 0-63 of P, R, X and O from warps 0, 1,
+// 4, 5, the "row warps"; state rows v from the warps of their quadrant):
+//   phase 1  all warps        k^, q^ (hi | lo), v, z, gates of the chunk's 64
+//                             tokens; the running sum G
 //   MMA 1                     P = K^ K^^T, R = Q^ K^^T, X = K^ S, O = Q^ S
-//   phase 2  warps 0,1        A from P; B = beta (v - e^G X) and O <- e^G O for
-//                             v < 64
-//            warps 4,5        R~ from R; the same for v >= 64
-//            all warps        S^T <- e^(G_last) S^T (their quadrant's rows, half
-//                             of the columns each)
+//   phase 2  row warps 0,1    A from P            row warps 4,5   R~ (hi | lo) from R
+//            row warps        B = beta (v - e^G X) and O <- e^G O (each half of v)
+//            warps 2,3,6,7    K~^T hi and lo, then the FP32 output gate w silu(z)
+//            all warps        S^T <- e^(G_last) S^T (their quadrant's state rows)
 //   phase 3  all warps        (I + A) V' = B: two threads per value column,
-//                             rows split by parity; the V'^T tile
+//                             rows split by parity; V'^T hi and lo tiles
 //   MMA 2                     O += R~ V',  S^T += V'^T K~
-//   phase 4  warps 0,1,4,5    the gated RMSNorm epilogue of the chunk's rows
-//                             (each warp half of the columns); then all warps
-//                             write the bf16 image of S^T for the next chunk
+//   phase 4  row warps        the gated RMSNorm of the chunk's rows (each warp
+//                             half of the columns); state images rows 0..63
+//            warps 2,3,6,7    state images rows 64..127; then all warps store
+//                             the output rows
 //
 // The state lives transposed in tensor memory (lane v, column kd), so its
-// bf16 image, the K-major [v][kd] operand, is written row by row.
+// images, the K-major [v][kd] operands, are written row by row.
 template <typename StateT>
 __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_chunked_kernel(const Params p) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -291,12 +332,14 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_chunked_kernel(const 
     Misc& ms = *reinterpret_cast<Misc*>(sm + kMisc);
     float* A2 = reinterpret_cast<float*>(sm + kA2);
     float* BT = reinterpret_cast<float*>(sm + kBT);
+    float* Gate = reinterpret_cast<float*>(sm + kGate);
     uint2* Zq = reinterpret_cast<uint2*>(sm + kZ);
     uint2* Stage = reinterpret_cast<uint2*>(sm + kBT);          // output rows, after the solve
     const uint32_t sbase = saddr(sm);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quad = warp & 3;                                  // TMEM lane quadrant of this warp
     const int half = warp >> 2;                                 // which half of the columns
+    const bool row_warp = quad < 2;                             // reaches the token rows 0-63
     const uint32_t lanes = static_cast<uint32_t>(quad * 32) << 16;
     const int row = quad * 32 + lane;                           // this thread's TMEM lane
     const int unit = static_cast<int>(blockIdx.x);
@@ -328,13 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_chunked_kernel(const 
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(saddr(&ms.bar)));
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    // rows 64-127 of the token-row tiles are zero for the whole prompt
-    for (int e = tid; e < 64 * 16; e += kThreads) {
-        const int r = 64 + (e >> 4), j = e & 15;
-        *reinterpret_cast<uint4*>(sm + kTileK + swz_chunk(r, j, 128)) = make_uint4(0, 0, 0, 0);
-        *reinterpret_cast<uint4*>(sm + kTileQ + swz_chunk(r, j, 128)) = make_uint4(0, 0, 0, 0);
-        if (j < 8) *reinterpret_cast<uint4*>(sm + kTileR + swz_chunk(r, j, 128)) = make_uint4(0, 0, 0, 0);
-    }
+    if (gated && tid < kV) ms.wn[tid] = __bfloat162float(p.norm_w[tid]);
     fence_before();
     __syncthreads();
     fence_after();
@@ -344,7 +381,18 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_chunked_kernel(const 
     uint32_t phase = 0;
     bool ok = true;
 
-    // ---- initial state: S^T (FP32) into TMEM lane v, its bf16 image into the S^T tile.
+    // hi and lo images of 32 FP32 state values (kd0 .. kd0 + 31 of row v)
+    auto put_images = [&](int v, int kd0, const float (&x)[32]) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            uint4 hi, lo;
+            split8(x + 8 * j, hi, lo);
+            *reinterpret_cast<uint4*>(sm + kTileS + swz_chunk(v, (kd0 >> 3) + j, 128)) = hi;
+            *reinterpret_cast<uint4*>(sm + kTileS2 + swz_chunk(v, (kd0 >> 3) + j, 128)) = lo;
+        }
+    };
+
+    // ---- initial state: S^T (FP32) into TMEM lane v, its images into the S^T tiles.
     //      Thread (v, half) covers kd in [64 half, 64 half + 64); a warp reads 32
     //      consecutive v of one kd row per load. ----
     {
@@ -358,9 +406,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_chunked_kernel(const 
 #pragma unroll
             for (int j = 0; j < 32; ++j) x[j] = src ? load_elem(src + (kd0 + j) * kV) : 0.f;
             tm_st32(tS + lanes + kd0, x);
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-                *reinterpret_cast<uint4*>(sm + kTileS + swz_chunk(row, (kd0 >> 3) + j, 128)) = pack8(x + 8 * j);
+            put_images(row, kd0, x);
         }
     }
 
@@ -396,14 +442,12 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_chunked_kernel(const 
         }
     };
     load_chunk(0);
-    float wv[4] = {0.f, 0.f, 0.f, 0.f};                          // this lane's 4 norm weights
-    if (gated) unpack4(__ldg(reinterpret_cast<const uint2*>(p.norm_w) + lane), wv);
 
     for (int c0 = 0; c0 < L; c0 += kC) {
         const int n = min(kC, L - c0);
 
-        // ---- phase 1: per token (8 per warp) k^, q^ (bf16 tiles), v (B^T), z, gates,
-        //      from the raw rows loaded while the previous chunk finished ----
+        // ---- phase 1: per token (8 per warp) k^, q^ (hi | lo), v (B^T), raw z,
+        //      gates, from the raw rows loaded while the previous chunk finished ----
         {
             // gates of the warp's 8 tokens, one per lane
             const float b_in = __shfl_down_sync(0xffffffffu, ab, 8);
@@ -438,27 +482,25 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_chunked_kernel(const 
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             const int t = warp + 8 * j;
-            uint2 kk = make_uint2(0, 0), qq = make_uint2(0, 0);
+            uint2 khi = make_uint2(0, 0), klo = khi, qhi = khi, qlo = khi;
             if (t < n) {
                 float qv[4], kv[4];
                 unpack4(qraw[j], qv);
                 unpack4(kraw[j], kv);
-                if (gated) {
-                    // the output gate w silu(z) of this lane's 4 columns, kept as bf16
-                    float zz[4];
-                    unpack4(zraw[j], zz);
-                    Zq[t * kZStride + lane] = make_uint2(pack_bf16x2(wv[0] * silu(zz[0]), wv[1] * silu(zz[1])),
-                                                         pack_bf16x2(wv[2] * silu(zz[2]), wv[3] * silu(zz[3])));
-                }
+                if (gated) Zq[t * kZStride + lane] = zraw[j];    // the output gate's input, exact
                 const float rq = rsqrtf(sums[j] + kQkEps) * p.scale;
                 const float rk = rsqrtf(sums[8 + j] + kQkEps);
-                kk = make_uint2(pack_bf16x2(kv[0] * rk, kv[1] * rk), pack_bf16x2(kv[2] * rk, kv[3] * rk));
-                qq = make_uint2(pack_bf16x2(qv[0] * rq, qv[1] * rq), pack_bf16x2(qv[2] * rq, qv[3] * rq));
+                split2(kv[0] * rk, kv[1] * rk, khi.x, klo.x);
+                split2(kv[2] * rk, kv[3] * rk, khi.y, klo.y);
+                split2(qv[0] * rq, qv[1] * rq, qhi.x, qlo.x);
+                split2(qv[2] * rq, qv[3] * rq, qhi.y, qlo.y);
 #pragma unroll
                 for (int e = 0; e < 4; ++e) BT[(lane + 32 * e) * kBStride + t] = __bfloat162float(vraw[j][e]);
             }
-            *reinterpret_cast<uint2*>(sm + kTileK + swz(t, lane * 4, 128)) = kk;
-            *reinterpret_cast<uint2*>(sm + kTileQ + swz(t, lane * 4, 128)) = qq;
+            *reinterpret_cast<uint2*>(sm + kTileK + swz(t, lane * 4, kC)) = khi;
+            *reinterpret_cast<uint2*>(sm + kTileK + swz(t, kK + lane * 4, kC)) = klo;
+            *reinterpret_cast<uint2*>(sm + kTileQ + swz(t, lane * 4, kC)) = qhi;
+            *reinterpret_cast<uint2*>(sm + kTileQ + swz(t, kK + lane * 4, kC)) = qlo;
         }
         __syncthreads();
         if (warp == 0) {
@@ -482,27 +524,17 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_chunked_kernel(const 
                 ms.kfac[t] = t < n ? expf(G_last - ms.G[t]) : 0.f;
             }
         }
-        __syncthreads();
-        // K~^T [kd][t] = k^_t[kd] e^(G_last - G_t): one 16-byte chunk (8 tokens) per item
-        for (int e = tid; e < kK * (kC / 8); e += kThreads) {
-            const int kd = e & (kK - 1), j = e >> 7;
-            float x[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int t = 8 * j + u;
-                x[u] = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(sm + kTileK + swz(t, kd, 128))) *
-                       ms.kfac[t];
-            }
-            *reinterpret_cast<uint4*>(sm + kTileKd + swz_chunk(kd, j, 128)) = pack8(x);
-        }
         sync_for_mma();
 
-        // ---- MMA 1: P = K^ K^^T, R = Q^ K^^T, X = K^ S, O = Q^ S ----
+        // ---- MMA 1: P = K^ K^^T, R = Q^ K^^T, X = K^ S, O = Q^ S (hi.hi + lo.hi +
+        //      hi.lo each) ----
         if (tid == 0) {
-            gemm(tP, sbase + kTileK, 128, sbase + kTileK, 128, 64, kK, false);
-            gemm(tX, sbase + kTileK, 128, sbase + kTileS, 128, 128, kK, false);
-            gemm(tO, sbase + kTileQ, 128, sbase + kTileS, 128, 128, kK, false);
-            gemm(tR, sbase + kTileQ, 128, sbase + kTileK, 128, 64, kK, false);
+            const uint32_t kH = sbase + kTileK, kL = kH + 2 * kC * 128;     // K^ hi | lo atom columns
+            const uint32_t qH = sbase + kTileQ, qL = qH + 2 * kC * 128;
+            gemm_split(tP, kH, kL, kC, kH, kL, kC, 64, kK, false);
+            gemm_split(tX, kH, kL, kC, sbase + kTileS, sbase + kTileS2, 128, 128, kK, false);
+            gemm_split(tO, qH, qL, kC, sbase + kTileS, sbase + kTileS2, 128, 128, kK, false);
+            gemm_split(tR, qH, qL, kC, kH, kL, kC, 64, kK, false);
             commit(bar);
         }
         ok = !__syncthreads_or(!wait_parity(bar, phase));
@@ -511,9 +543,9 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_chunked_kernel(const 
         fence_after();
 
         // ---- phase 2 ----
-        if (quad < 2) {
+        if (row_warp) {
             const int t = row;                                  // token row of this lane
-            const float Gt = ms.G[t], bt = ms.beta[t];
+            const float Gt = ms.G[t], bt = ms.beta[t], eG = ms.eG[t];
             const bool live = t < n;
             if (half == 0) {
                 // A (s < t) from P, stored as A2[s][t % 2][t / 2]; the decay
@@ -532,7 +564,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_chunked_kernel(const 
                     }
                 }
             } else {
-                // R~ (s <= t) from R
+                // R~ (s <= t) from R, hi | lo
 #pragma unroll
                 for (int s0 = 0; s0 < kC; s0 += 32) {
                     float x[32], d[32];
@@ -544,12 +576,15 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_chunked_kernel(const 
                         x[u] = (live && s <= t) ? d[u] * x[u] : 0.f;
                     }
 #pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        *reinterpret_cast<uint4*>(sm + kTileR + swz_chunk(t, (s0 >> 3) + j, 128)) = pack8(x + 8 * j);
+                    for (int j = 0; j < 4; ++j) {
+                        uint4 hi, lo;
+                        split8(x + 8 * j, hi, lo);
+                        *reinterpret_cast<uint4*>(sm + kTileR + swz_chunk(t, (s0 >> 3) + j, kC)) = hi;
+                        *reinterpret_cast<uint4*>(sm + kTileR + swz_chunk(t, 8 + (s0 >> 3) + j, kC)) = lo;
+                    }
                 }
             }
             // B = beta (v - e^(G_t) X) and O <- e^(G_t) O for this half of the value columns
-            const float eG = ms.eG[t];
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
                 const int v0 = 64 * half + 32 * c;
@@ -564,6 +599,42 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_chunked_kernel(const 
 #pragma unroll
                 for (int u = 0; u < 32; ++u) x[u] *= eG;
                 tm_st32(tO + lanes + v0, x);
+            }
+        } else {
+            // K~^T [kd][t] = k^_t[kd] e^(G_last - G_t) (k^ = hi + lo), split again:
+            // one 16-byte chunk (8 tokens) of each part per item (the Q^ region,
+            // free since MMA 1)
+            const int wt = tid - 64 * (1 + half);              // 0..127 over warps 2, 3, 6, 7
+            for (int e = wt; e < kK * (kC / 8); e += 128) {
+                const int kd = e & (kK - 1), j = e >> 7;
+                float x[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int t = 8 * j + u;
+                    const float kv =
+                        __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(sm + kTileK + swz(t, kd, kC))) +
+                        __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(sm + kTileK + swz(t, kK + kd, kC)));
+                    x[u] = kv * ms.kfac[t];
+                }
+                uint4 hi, lo;
+                split8(x, hi, lo);
+                *reinterpret_cast<uint4*>(sm + kTileKdHi + swz_chunk(kd, j, 128)) = hi;
+                *reinterpret_cast<uint4*>(sm + kTileKdLo + swz_chunk(kd, j, 128)) = lo;
+            }
+            // every K^ read above is done before the gate overwrites the region
+            asm volatile("bar.sync 1, 128;" ::: "memory");
+            if (gated) {
+                // the output gate w silu(z) in FP32, [t][v ^ (t % 32)]
+                for (int e = wt; e < kC * (kV / 4); e += 128) {
+                    const int t = e >> 5, q4 = e & 31;
+                    float zz[4];
+                    unpack4(Zq[t * kZStride + q4], zz);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const int v = 4 * q4 + c;
+                        Gate[t * kV + (v ^ (t & 31))] = ms.wn[v] * silu(zz[c]);
+                    }
+                }
             }
         }
         {
@@ -605,17 +676,23 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_chunked_kernel(const 
                     fma2(x[4 * i4 + 2], x[4 * i4 + 3], a4.z, a4.w, nxs);
                 }
             }
-            // V'^T tile row vc: this thread's tokens 2 i + r
+            // V'^T tile rows vc, hi and lo: this thread's tokens 2 i + r
 #pragma unroll
-            for (int i2 = 0; i2 < 32; ++i2)
-                *reinterpret_cast<__nv_bfloat16*>(sm + kTileV + swz(vc, 2 * i2 + r, 128)) = __float2bfloat16_rn(x[i2]);
+            for (int i2 = 0; i2 < 32; ++i2) {
+                const __nv_bfloat16 hi = __float2bfloat16_rn(x[i2]);
+                const __nv_bfloat16 lo = __float2bfloat16_rn(x[i2] - __bfloat162float(hi));
+                *reinterpret_cast<__nv_bfloat16*>(sm + kTileVHi + swz(vc, 2 * i2 + r, 128)) = hi;
+                *reinterpret_cast<__nv_bfloat16*>(sm + kTileVLo + swz(vc, 2 * i2 + r, 128)) = lo;
+            }
         }
         sync_for_mma();
 
         // ---- MMA 2: O += R~ V',  S^T += V'^T K~; meanwhile the next chunk's loads ----
         if (tid == 0) {
-            gemm(tO, sbase + kTileR, 128, sbase + kTileV, 128, 128, kC, true);
-            gemm(tS, sbase + kTileV, 128, sbase + kTileKd, 128, 128, kC, true);
+            const uint32_t rH = sbase + kTileR, rL = rH + kC * 128;          // R~ hi | lo atom columns
+            gemm_split(tO, rH, rL, kC, sbase + kTileVHi, sbase + kTileVLo, 128, 128, kC, true);
+            gemm_split(tS, sbase + kTileVHi, sbase + kTileVLo, 128, sbase + kTileKdHi, sbase + kTileKdLo, 128,
+                       128, kC, true);
             commit(bar);
         }
         if (c0 + kC < L) load_chunk(c0 + kC);
@@ -624,9 +701,10 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_chunked_kernel(const 
         if (!ok) break;
         fence_after();
 
-        // ---- phase 4: outputs (rows t < 64 on warps 0, 1, 4, 5; each warp half of
-        //      the columns), then the bf16 image of S^T for the next chunk ----
-        if (quad < 2 && gated) {
+        // ---- phase 4: outputs (rows t < 64 on the row warps; each warp half of
+        //      the columns), then the state images for the next chunk ----
+        const bool more = c0 + kC < L;
+        if (row_warp && gated) {
             float ss = 0.f;
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
@@ -637,45 +715,34 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_chunked_kernel(const 
             }
             ms.ssq[half][row] = ss;
         }
-        const bool more = c0 + kC < L;
-        if (more && quad >= 2) {
-            // image rows v = 64..127 while the others wait for the norms
+        if (more && !row_warp) {
+            // images of rows v = 64..127 while the others wait for the norms
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
                 const int kd0 = 64 * half + 32 * c;
                 float x[32];
                 tm_ld32(tS + lanes + kd0, x);
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    *reinterpret_cast<uint4*>(sm + kTileS + swz_chunk(row, (kd0 >> 3) + j, 128)) = pack8(x + 8 * j);
+                put_images(row, kd0, x);
             }
         }
         __syncthreads();
-        if (quad < 2) {
+        if (row_warp) {
             // normalised, gated rows into the staging buffer (the B^T region,
-            // free until the next chunk), then the image rows v = 0..63
+            // free until the next chunk), then the images of rows v = 0..63
             const int t = row;
             const float rinv = gated ? rsqrtf((ms.ssq[0][t] + ms.ssq[1][t]) * (1.0f / kV) + p.eps) : 1.0f;
             uint2* srow = Stage + t * kStagePitch + 16 * half;
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
                 float x[32];
-                uint2 gq[8];
-                if (gated) {
-#pragma unroll
-                    for (int j4 = 0; j4 < 8; ++j4) gq[j4] = Zq[t * kZStride + 16 * half + 8 * c + j4];
-                }
                 tm_ld32(tO + lanes + 64 * half + 32 * c, x);
 #pragma unroll
                 for (int j4 = 0; j4 < 8; ++j4) {
                     float y[4];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) y[e] = x[4 * j4 + e];
-                    if (gated) {
-                        float gg[4];
-                        unpack4(gq[j4], gg);
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) y[e] = y[e] * rinv * gg[e];
+                    for (int e = 0; e < 4; ++e) {
+                        const int v = 64 * half + 32 * c + 4 * j4 + e;
+                        y[e] = gated ? x[4 * j4 + e] * rinv * Gate[t * kV + (v ^ (t & 31))] : x[4 * j4 + e];
                     }
                     srow[8 * c + j4] = make_uint2(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]));
                 }
@@ -686,9 +753,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_chunked_kernel(const 
                     const int kd0 = 64 * half + 32 * c;
                     float x[32];
                     tm_ld32(tS + lanes + kd0, x);
-#pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        *reinterpret_cast<uint4*>(sm + kTileS + swz_chunk(row, (kd0 >> 3) + j, 128)) = pack8(x + 8 * j);
+                    put_images(row, kd0, x);
                 }
             }
         }

@@ -249,10 +249,12 @@ GDNSPEC_API gdn_status gdn_prefill(
  *     o_t = e^(G_t) S^T q^_t + sum_{s <= t} e^(G_t - G_s) (q^_t.k^_s) v'_s
  *     S  <- e^(G_last) S + sum_s e^(G_last - G_s) k^_s v'_s^T
  * which is the same quantity as the token recurrence, in exact arithmetic.
- * The products take bf16 operands with FP32 accumulation (k^, q^, the bf16
- * image of S, the decay-weighted scores and V'); the carried state, the
- * triangular solve and the epilogue are FP32.  The state is rounded to the
- * pool dtype once, when it is stored at the end of the prompt.
+ * The products run on the tensor cores at FP32 accuracy: each operand is
+ * carried as a bf16 hi part and a bf16 lo part (hi + lo within 2^-18 of the
+ * FP32 value) and the hi.hi, lo.hi and hi.lo products accumulate in FP32; the
+ * carried state, the triangular solve and the epilogue are FP32.  The state
+ * is rounded to the pool dtype once, when it is stored at the end of the
+ * prompt.
  *
  * Arguments, layouts, the caller contract and the status bits are those of
  * gdn_prefill; in addition GDN_FLAG_TIMEOUT reports a tensor-core wait that

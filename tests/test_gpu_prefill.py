@@ -4,16 +4,13 @@ through the C-ABI) with the oracle's prefill routine: the same per-token step
 over whole prompts, the state carried from a slot (or the zero state) and
 stored once at the end (PR #52191 report, implementation steps 3-4).
 
-Tolerances.  The recurrent path computes in FP32 like the decode step and is
-held to the decode step's bounds (PR #51674 report, step 5: output rel L2
-< 5e-4; FP32 state the same; narrow states atol = rtol = 3e-2).  The chunked
-path feeds the tensor cores bf16 operands (k^, q^, the bf16 image of the
-state, the decay-weighted scores and the solved V'), each carrying a relative
-rounding error of at most 2^-9 ~ 2e-3; a product of two such operands and a
-sum over independent terms gives about 2e-3 relative in L2, and the solve and
-the two-term readout keep it of that order.  Its bound is 1e-2 in rel L2
-(the PR #52191 report's kernel checks use atol 1e-2), five times that
-estimate; narrow states keep atol = rtol = 3e-2.
+Tolerances.  Both paths are held to the decode step's bounds (PR #51674
+report, step 5: output rel L2 < 5e-4; FP32 state the same; narrow states
+atol = rtol = 3e-2).  The recurrent path computes in FP32 like the decode
+step.  The chunked path runs its products on the tensor cores at FP32
+accuracy (PR #52191 report, step 4: the chunk products on FP32 buffers):
+every operand is carried as a bf16 hi part and a bf16 lo part, so each
+product is formed to about 2^-17 relative before FP32 accumulation.
 """
 from __future__ import annotations
 
@@ -36,7 +33,8 @@ DEV = torch.device("cuda", 0)
 THREADS = os.cpu_count() or 1
 
 # entry point -> rel L2 bound for outputs and FP32 states
-ENTRIES = {"recurrent": (gdn.gdn_prefill, 5e-4), "chunked": (gdn.gdn_prefill_chunked, 1e-2)}
+ENTRIES = {"recurrent": (gdn.gdn_prefill, 5e-4), "chunked": (gdn.gdn_prefill_chunked, 5e-4)}
+ERRORS = []         # (test, entry, out rel L2, FP32-state rel L2), printed at the end of the module
 WEAK_DECAY = (1e-3, 5e-2)
 
 
@@ -85,6 +83,11 @@ def _check(entry, case, out, pool, st, ref, host, writes):
     w = bf16_values(ref["out_bf16"])
     assert np.all(np.isfinite(g))
     err_out = rel_l2(g, w)
+    err_state = None
+    if case.state_dtype == synth.F32:
+        wr0 = [int(s) for s in writes if s >= 0]
+        err_state = rel_l2(state_values(to_host_bits(pool), case.state_dtype)[wr0], state_values(host, case.state_dtype)[wr0])
+    ERRORS.append((os.environ.get("PYTEST_CURRENT_TEST", "").split(" ")[0], entry, err_out, err_state))
     assert err_out < tol, err_out
     gp = state_values(to_host_bits(pool), case.state_dtype)
     wp = state_values(host, case.state_dtype)
@@ -233,3 +236,9 @@ def test_input_extremes(entry):
     ext = dataclasses.replace(case, a=bf16_bits(a), b=bf16_bits(b), z=bf16_bits(z), q=bf16_bits(q), k=bf16_bits(k))
     reads, writes = _slots(ext, 7, zero_every=10 ** 6, skip_every=10 ** 6)
     _check(entry, ext, *_run(entry, ext, reads, writes), writes)
+
+
+def test_zz_report_errors():
+    """Prints the measured errors of every comparison above (run with -s)."""
+    for name, entry, e_out, e_state in ERRORS:
+        print(f"{entry:10s} out {e_out:.3e} state {e_state if e_state is None else f'{e_state:.3e}'}  {name}")
