@@ -50,7 +50,7 @@ FLUSH_BYTES = 512 << 20
 N_WINDOWS = 64
 N_COLD = 64
 
-GDN_PRE_INDEX, GDN_PRE_TOKENS = 0x1, 0x2
+GDN_PRE_INDEX, GDN_PRE_TOKENS, GDN_PRE_STATE = 0x1, 0x2, 0x4
 
 # name: (description, spec)
 WORKLOADS = {
@@ -868,9 +868,10 @@ def main():
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="bs32_t8_bf16")
     ap.add_argument("--split", type=lambda x: int(x, 0), default=0,
                     help="decode workloads: dims.split (0 = the library's choice; 1, 2, 4, 8, 0x102, 0x104)")
-    ap.add_argument("--flags", type=lambda x: int(x, 0), default=GDN_PRE_INDEX | GDN_PRE_TOKENS,
-                    help="decode workloads: dims.flags (default 3 = GDN_PRE_INDEX | GDN_PRE_TOKENS: the resident "
-                         "inputs are not written by the preceding kernel; the conv workload keeps the index bit)")
+    ap.add_argument("--flags", type=lambda x: int(x, 0), default=GDN_PRE_INDEX | GDN_PRE_TOKENS | GDN_PRE_STATE,
+                    help="decode workloads: dims.flags (default 7 = GDN_PRE_INDEX | GDN_PRE_TOKENS | GDN_PRE_STATE: "
+                         "the resident inputs and the rotating sets' disjoint slots are not written by the preceding "
+                         "step; the conv workload keeps the index bit)")
     ap.add_argument("--prefill-form", choices=("chunked", "recurrent"), default="chunked",
                     help="prefill workloads: gdn_prefill_chunked (tensor cores) or gdn_prefill (per token)")
     args = ap.parse_args()

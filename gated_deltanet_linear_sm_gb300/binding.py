@@ -25,6 +25,7 @@ GDN_FLAG_TIMEOUT = 16
 GDN_SPLIT_NARROW = 0x100     # dims.split flag: 8 V columns per warp (small batches)
 GDN_PRE_INDEX = 0x1          # dims.flags: the index tables were not written by the preceding kernel
 GDN_PRE_TOKENS = 0x2         # dims.flags (with GDN_PRE_INDEX): nor were the token inputs
+GDN_PRE_STATE = 0x4          # dims.flags (with GDN_PRE_INDEX): nor were the state slots this call reads
 
 
 class gdn_dims(ctypes.Structure):
@@ -193,8 +194,9 @@ def gdn_spec_decode(q, k, v, a, b, z, A_log, dt_bias, norm_w, state_pool, state_
     state_pool [num_slots, H_v, 128, 128] fp32 / bf16 / fp16 (updated in
     place); state_indices [B, spec_stride], num_accepted [B], cu_seqlens
     [B+1], spec_token_indx [sum q_len] (optional) and status [1] (optional)
-    int32.  ``flags``: GDN_PRE_INDEX [| GDN_PRE_TOKENS] when those inputs were
-    not written by the kernel launched just before on the stream.  Launches on
+    int32.  ``flags``: GDN_PRE_INDEX [| GDN_PRE_TOKENS] [| GDN_PRE_STATE] when
+    those inputs were not written by the kernel launched just before on the
+    stream.  Launches on
     ``stream`` (default: the current stream) and returns ``out``."""
     call = prepare(q, k, v, a, b, z, A_log, dt_bias, norm_w, state_pool, state_indices,
                    num_accepted, cu_seqlens, out, spec_token_indx=spec_token_indx, scale=scale,

@@ -39,7 +39,7 @@ struct Params {
     int64_t q_stride, k_stride, v_stride, a_stride, b_stride, z_stride, out_stride;
     int64_t num_slots;
     int32_t batch, num_tokens, H_k, H_v, stride, max_T, group;
-    int32_t flags;                   // decode: GDN_PRE_INDEX / GDN_PRE_TOKENS (inputs read before the dependency wait)
+    int32_t flags;                   // decode: GDN_PRE_* (inputs read before the dependency wait)
     float scale, eps;
     // short causal convolution in front of the step (gdn_spec_decode_conv only)
     const __nv_bfloat16* x;          // pre-convolution rows, channels q | k | v

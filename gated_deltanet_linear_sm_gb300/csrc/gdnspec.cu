@@ -618,13 +618,15 @@ gdn_spec_decode_kernel(const __grid_constant__ Params p) {
     // visible before it touches memory the grid may have written, then lets
     // the next kernel's CTAs be scheduled.  By default the wait comes before
     // the first global access; GDN_PRE_INDEX moves it after the index reads,
-    // GDN_PRE_TOKENS (with it) after the token prologue as well, so that those
-    // reads overlap the previous grid's tail.  The state tile, out, the conv
-    // slots and the status word are touched only after the wait; every exit
-    // waits first, so that no successor is released before this grid's
-    // predecessor has completed.
+    // GDN_PRE_TOKENS (with it) after the token prologue as well and
+    // GDN_PRE_STATE (with it) after the state tile's load, so that those reads
+    // overlap the previous grid's tail.  Every write (slots, out, the conv
+    // slots, the status word) comes after the wait; every exit waits first, so
+    // that no successor is released before this grid's predecessor has
+    // completed.
     const bool pre_index = (p.flags & GDN_PRE_INDEX) != 0;
     const bool pre_tokens = !CONV && pre_index && (p.flags & GDN_PRE_TOKENS) != 0;
+    const bool pre_state = !CONV && pre_index && (p.flags & GDN_PRE_STATE) != 0;
     bool waited = false;
     auto dep_wait = [&]() {
         if (!waited) {
@@ -674,18 +676,19 @@ gdn_spec_decode_kernel(const __grid_constant__ Params p) {
             return;
         }
     }
-    if (!pre_tokens) dep_wait();
-
     // ---- load this lane's R x 4 block of the state tile (FP32 in registers):
     //      rows rg + G r, columns col0 .. col0 + 3; issued before the token
-    //      prologue, or after it when the prologue runs ahead of the wait ----
+    //      prologue (ahead of the wait with GDN_PRE_STATE), or after the
+    //      prologue when only the prologue runs ahead of the wait ----
     const StateT* src = static_cast<const StateT*>(p.pool) + (rs * p.H_v + h) * kTile;
     float S[L::kRows][4];
-    if (!pre_tokens) {
+    if (!pre_state && !pre_tokens) dep_wait();
+    if (pre_state || !pre_tokens) {
 #pragma unroll
         for (int r = 0; r < L::kRows; ++r)
             StateIO<StateT>::load4(src + static_cast<int64_t>(rg + L::kRowGroups * r) * kV + col0, S[r]);
     }
+    if (pre_state && !pre_tokens) dep_wait();
 
     // ---- per-token prologue: gather rows, gates, normalised q / k, v, z ----
     const int kh = h / p.group;
@@ -724,9 +727,11 @@ gdn_spec_decode_kernel(const __grid_constant__ Params p) {
     }
     if (pre_tokens) {
         dep_wait();
+        if (!pre_state) {
 #pragma unroll
-        for (int r = 0; r < L::kRows; ++r)
-            StateIO<StateT>::load4(src + static_cast<int64_t>(rg + L::kRowGroups * r) * kV + col0, S[r]);
+            for (int r = 0; r < L::kRows; ++r)
+                StateIO<StateT>::load4(src + static_cast<int64_t>(rg + L::kRowGroups * r) * kV + col0, S[r]);
+        }
     }
     // publishes the prologue; every CTA of the cluster checks every token row,
     // so the skip decision below is the same in all of them
@@ -966,7 +971,8 @@ int choose_split(int64_t units, gdn_dtype dt) {
 gdn_status check_dims(const gdn_dims* d) {
     if (d == nullptr) return GDN_ERR_NULL_ARG;
     if (d->batch < 0 || d->num_tokens < 0 || d->H_k <= 0 || d->H_v <= 0 || d->spec_stride < 1 ||
-        d->num_slots < 1 || d->H_v % d->H_k != 0 || (d->flags & ~(GDN_PRE_INDEX | GDN_PRE_TOKENS)) != 0)
+        d->num_slots < 1 || d->H_v % d->H_k != 0 ||
+        (d->flags & ~(GDN_PRE_INDEX | GDN_PRE_TOKENS | GDN_PRE_STATE)) != 0)
         return GDN_ERR_BAD_SHAPE;
     if (d->max_T < 1 || d->max_T > kMaxT) return GDN_ERR_BAD_SHAPE;
     if (d->q_stride < 0 || d->k_stride < 0 || d->v_stride < 0 || d->a_stride < 0 || d->b_stride < 0 ||
@@ -1122,7 +1128,7 @@ gdn_status gdn_spec_decode_conv(const void* x, const void* conv_weight, const vo
         static_cast<int64_t>(cdims->state_len) < cdims->width - 1 + static_cast<int64_t>(dims->spec_stride))
         return GDN_ERR_BAD_SHAPE;
     if (state_dtype != GDN_F32 && state_dtype != GDN_BF16 && state_dtype != GDN_F16) return GDN_ERR_UNSUPPORTED;
-    if (dims->split > 1 || (dims->flags & GDN_PRE_TOKENS)) return GDN_ERR_UNSUPPORTED;
+    if (dims->split > 1 || (dims->flags & (GDN_PRE_TOKENS | GDN_PRE_STATE))) return GDN_ERR_UNSUPPORTED;
     if (dims->batch == 0) return GDN_OK;
     if (!state_indices || !num_accepted || !x || !conv_weight || !conv_pool || !conv_in || !conv_out)
         return GDN_ERR_NULL_ARG;

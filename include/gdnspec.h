@@ -49,7 +49,7 @@ extern "C" {
 #endif
 
 /* 2: gdn_spec_decode_split takes the state dtype; dims->split accepts GDN_SPLIT_NARROW
-   3: dims->flags (formerly reserved): GDN_PRE_INDEX, GDN_PRE_TOKENS */
+   3: dims->flags (formerly reserved): GDN_PRE_INDEX, GDN_PRE_TOKENS, GDN_PRE_STATE */
 #define GDNSPEC_VERSION 3
 
 #if defined(__GNUC__)
@@ -106,18 +106,25 @@ typedef enum { GDN_F32 = 0, GDN_BF16 = 1, GDN_F16 = 2 } gdn_dtype;
  *                   (for example: they were filled at the start of the step);
  *   GDN_PRE_TOKENS  with GDN_PRE_INDEX: neither were q, k, v, a, b, z, A_log,
  *                   dt_bias and norm_w (for example: the batch's inputs are
- *                   resident and the preceding kernel is another decode step).
- * The state pool, out and status_word are always accessed after the wait, so
- * back-to-back steps that rewind into each other's slots stay ordered.  A
+ *                   resident and the preceding kernel is another decode step);
+ *   GDN_PRE_STATE   with GDN_PRE_INDEX: nor were the state slots this call
+ *                   reads (the rewound slots).  True in a model's forward
+ *                   pass, where the kernel before a layer's step is never that
+ *                   layer's own step; false for two steps of one layer in a
+ *                   row where the second rewinds into the first's slots.
+ * out, status_word and every slot write are accessed after the wait; without
+ * GDN_PRE_STATE so is the state read, so back-to-back steps that rewind into
+ * each other's slots stay ordered.  A
  * decode launch signals its successor only after its own wait, so when the
  * preceding kernel is one of this library's decode launches, or a kernel that
  * does not use programmatic dependent launch, every kernel before it has
  * completed when the early reads happen.
- * gdn_spec_decode_conv accepts GDN_PRE_INDEX only; the prefill entry points
- * take no flags.
+ * gdn_spec_decode_conv accepts GDN_PRE_INDEX only (its conv history may be
+ * the preceding step's output); the prefill entry points take no flags.
  */
 #define GDN_PRE_INDEX  0x1
 #define GDN_PRE_TOKENS 0x2
+#define GDN_PRE_STATE  0x4
 
 /* Opaque CUDA stream handle; the same type as cudaStream_t (NULL = legacy default stream). */
 typedef struct CUstream_st* gdn_stream_t;
@@ -142,7 +149,7 @@ typedef struct {
                              (each warp owns 16 V columns), or GDN_SPLIT_NARROW
                              | 2 or | 4 (each warp owns 8 V columns: 16 warps
                              per unit over 2 or 4 CTAs) */
-    int32_t flags;        /* 0, or GDN_PRE_INDEX [| GDN_PRE_TOKENS] (above); 0 for the prefill entry points */
+    int32_t flags;        /* 0, or GDN_PRE_INDEX [| GDN_PRE_TOKENS] [| GDN_PRE_STATE] (above); 0 for prefill */
 } gdn_dims;
 
 /*

@@ -97,7 +97,7 @@ def _call(lib, dims, *, ptr=0x1000, z=0x1000, w=0x1000, state_dtype=0):
     (dict(K=64), 3), (dict(V=256), 3), (dict(H_v=12, H_k=8), 2), (dict(max_T=9), 2),
     (dict(max_T=0), 2), (dict(spec_stride=0), 2), (dict(batch=-1), 2), (dict(num_slots=0), 2),
     (dict(split=3), 3), (dict(split=0x101), 3), (dict(split=0x108), 3), (dict(split=0x100), 3),
-    (dict(flags=4), 2), (dict(flags=-1), 2), (dict(q_stride=-4), 2),
+    (dict(flags=8), 2), (dict(flags=-1), 2), (dict(q_stride=-4), 2),
 ])
 def test_bad_dims_rejected(lib, over, code):
     assert _call(lib, _dims(**over)) == code
@@ -166,6 +166,7 @@ def test_conv_bad_pointers_rejected(lib):
     assert _call_conv(lib, _dims(split=binding.GDN_SPLIT_NARROW | 2), _cdims()) == 3
     # the conv history may be the preceding step's output: token inputs are never read early
     assert _call_conv(lib, _dims(flags=binding.GDN_PRE_INDEX | binding.GDN_PRE_TOKENS), _cdims()) == 3
+    assert _call_conv(lib, _dims(flags=binding.GDN_PRE_INDEX | binding.GDN_PRE_STATE), _cdims()) == 3
     assert _call_conv(lib, _dims(batch=0), _cdims(), ptr=0) == 0  # empty batch: nothing launched
     assert lib.gdn_spec_decode_conv(*([None] * 6), None, *([None] * 12), ctypes.byref(_dims()), 0.1, 1e-5, 0,
                                     None, None) == 1

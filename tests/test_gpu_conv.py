@@ -106,6 +106,15 @@ def test_state_dtypes(sd):
     Step(case, synth.conv_inputs(case, seed=11)).run().check()
 
 
+@pytest.mark.parametrize("ratio", [1, 2, 3, 4, 8])
+def test_head_ratios(ratio):
+    """H_v = ratio * H_k: ratios 2, 4 and 8 share the key head's q / k
+    convolution over a cluster of its v-heads (each CTA convolves a slice and
+    the cluster exchanges them); 1 and 3 convolve q / k in every CTA."""
+    case = _case(batch=5, H_k=2, H_v=2 * ratio, seed=90 + ratio)
+    Step(case, synth.conv_inputs(case, seed=14 + ratio)).run().check()
+
+
 def test_zero_history_and_skipped_conv_writes():
     case = _case(batch=8, seed=83)
     ci = synth.conv_inputs(case, seed=12)

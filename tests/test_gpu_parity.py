@@ -217,7 +217,7 @@ def test_packed_mixed_qkv_strides(cuda_device):
     compare(case, out, pool)
 
 
-@pytest.mark.parametrize("flags", [0, 3])
+@pytest.mark.parametrize("flags", [0, 3, 7])
 def test_graph_capture_replays(cuda_device, flags):
     """A call captured in a CUDA graph and replayed gives the same bits as an
     eager call on the same inputs (the launch needs no host sync)."""
@@ -287,15 +287,15 @@ def test_gate_and_input_extremes(cuda_device, split):
 @pytest.mark.parametrize("split", [1, 2, 0x102])
 @pytest.mark.parametrize("sd", [synth.F32, synth.BF16])
 def test_early_read_flags_change_no_bit(cuda_device, sd, split):
-    """GDN_PRE_INDEX and GDN_PRE_INDEX | GDN_PRE_TOKENS move reads ahead of the
-    dependency wait; the results (out and every pool byte) are bit-identical to
-    flags = 0, on a ragged, padded batch."""
+    """GDN_PRE_INDEX, with GDN_PRE_TOKENS and / or GDN_PRE_STATE, moves reads
+    ahead of the dependency wait; the results (out and every pool byte) are
+    bit-identical to flags = 0, on a ragged, padded batch."""
     import gated_deltanet_linear_sm_gb300 as gdn
     case = synth.make_case(batch=24, H_k=2, H_v=16, T=8, state_dtype=sd, num_slots=400, q_lens="ragged",
                            pad_prob=0.1, seed=31)
     pool0 = make_pool(case, cuda_device)
     res = []
-    for flags in (0, gdn.binding.GDN_PRE_INDEX, gdn.binding.GDN_PRE_INDEX | gdn.binding.GDN_PRE_TOKENS):
+    for flags in (0, 1, 3, 5, 7):
         out, pool, st = run_gpu(case, cuda_device, pool0.clone(), split=split, flags=flags)
         torch.cuda.synchronize()
         assert int(st.item()) == 0
@@ -303,3 +303,29 @@ def test_early_read_flags_change_no_bit(cuda_device, sd, split):
         res.append((out.view(torch.int16).clone(), pool.view(dt).clone()))
     for r in res[1:]:
         assert torch.equal(r[0], res[0][0]) and torch.equal(r[1], res[0][1])
+
+
+def test_early_state_reads_between_independent_steps(cuda_device):
+    """GDN_PRE_STATE across back-to-back steps whose slots are disjoint (the
+    second step's rewound slots were not written by the first): both match
+    the oracle, as with flags = 0."""
+    from oracle import oracle as orc
+    from tests.util import bf16_values, initial_pool
+    case1 = synth.make_case(batch=8, H_k=1, H_v=8, T=4, state_dtype=synth.F32, num_slots=96, seed=32)
+    case2 = synth.make_case(batch=8, H_k=1, H_v=8, T=4, state_dtype=synth.F32, num_slots=96, seed=33)
+    free = np.setdiff1d(np.arange(96), case1.state_indices.ravel())
+    case2.state_indices = np.random.default_rng(4).choice(free, size=case2.state_indices.shape,
+                                                          replace=False).astype(np.int32)
+    pool = make_pool(case1, cuda_device, slots=np.union1d(case1.touched_slots(), case2.touched_slots()))
+    hp = initial_pool(case1)
+    hp[case2.touched_slots()] = case1.slot_values(case2.touched_slots())     # make_pool fills them so
+    t2 = device_tensors(case2, cuda_device)
+    out1, pool, _ = run_gpu(case1, cuda_device, pool, flags=7)
+    out2, pool, _ = run_gpu(case2, cuda_device, pool, flags=7, tensors=t2)
+    torch.cuda.synchronize()
+    r1 = orc.run_case(case1, hp)
+    r2 = orc.run_case(case2, hp)
+    for out, r in ((out1, r1), (out2, r2)):
+        g = bf16_values(out.view(torch.int16).cpu().numpy().view(np.uint16))
+        w = bf16_values(r["out_bf16"])
+        assert np.linalg.norm(g - w) / np.linalg.norm(w) < 5e-4
