@@ -22,6 +22,7 @@ GDN_FLAG_ACCEPTED = 2
 GDN_FLAG_QLEN = 4
 GDN_FLAG_TOKEN_ROW = 8
 GDN_FLAG_TIMEOUT = 16
+GDN_FLAG_DRAIN = 32
 GDN_SPLIT_NARROW = 0x100     # dims.split flag: 8 V columns per warp (small batches)
 GDN_PRE_INDEX = 0x1          # dims.flags: the index tables were not written by the preceding kernel
 GDN_PRE_TOKENS = 0x2         # dims.flags (with GDN_PRE_INDEX): nor were the token inputs
@@ -79,6 +80,7 @@ EXPORTS = {
     "gdn_spec_decode_conv": (ctypes.c_int, [_VP] * 6 + [ctypes.POINTER(gdn_conv_dims)] + [_VP] * 12 +
                              [ctypes.POINTER(gdn_dims), ctypes.c_float, ctypes.c_float, ctypes.c_int, _VP, _VP]),
     "gdn_spec_decode_split": (ctypes.c_int32, [ctypes.POINTER(gdn_dims), ctypes.c_int]),
+    "gdn_set_wait_limit": (None, [ctypes.c_uint32]),
     "gdn_status_str": (ctypes.c_char_p, [ctypes.c_int]),
     "gdn_version": (ctypes.c_int32, []),
 }
@@ -112,6 +114,12 @@ def status_str(status: int) -> str:
 
 def version() -> int:
     return int(load_library().gdn_version())
+
+
+def set_wait_limit(polls: int) -> None:
+    """Bound on each tensor-core wait of gdn_prefill_chunked, in polls (0: the
+    default); process-wide, for exercising the timeout path."""
+    load_library().gdn_set_wait_limit(int(polls))
 
 
 def _ptr(t):

@@ -40,6 +40,7 @@ struct Params {
     int64_t num_slots;
     int32_t batch, num_tokens, H_k, H_v, stride, max_T, group;
     int32_t flags;                   // decode: GDN_PRE_* (inputs read before the dependency wait)
+    uint32_t wait_limit;             // chunked prefill: polls per tensor-core wait (0: the default)
     float scale, eps;
     // short causal convolution in front of the step (gdn_spec_decode_conv only)
     const __nv_bfloat16* x;          // pre-convolution rows, channels q | k | v
@@ -51,6 +52,9 @@ struct Params {
     int64_t x_stride, num_conv_slots;
     int32_t conv_dim, conv_width, conv_state_len;
 };
+
+// Process-wide bound on the chunked prefill's tensor-core waits (0: the default).
+extern uint32_t g_wait_limit;
 
 // Launch the chunked prefill kernel: one CTA per (sequence, v-head) unit.
 cudaError_t launch_prefill_chunked(const Params& p, int64_t units, gdn_dtype state_dtype, cudaStream_t stream);

@@ -193,8 +193,8 @@ __device__ __forceinline__ void commit(uint32_t bar) {
                  : "memory");
 }
 
-__device__ __forceinline__ bool wait_parity(uint32_t bar, uint32_t parity) {
-    for (uint32_t it = 0; it < kSpinLimit; ++it) {
+__device__ __forceinline__ bool wait_parity(uint32_t bar, uint32_t parity, uint32_t limit) {
+    for (uint32_t it = 0; it < limit; ++it) {
         uint32_t done;
         asm volatile(
             "{\n\t.reg .pred P;\n\tmbarrier.try_wait.parity.shared::cta.b64 P, [%1], %2;\n\t"
@@ -205,6 +205,28 @@ __device__ __forceinline__ bool wait_parity(uint32_t bar, uint32_t parity) {
         if (done) return true;
     }
     return false;
+}
+
+// the same wait with non-blocking polls (mbarrier.test_wait): a bound set by
+// gdn_set_wait_limit counts these, so that a small bound runs out for certain
+__device__ __forceinline__ bool test_parity(uint32_t bar, uint32_t parity, uint32_t limit) {
+    for (uint32_t it = 0; it < limit; ++it) {
+        uint32_t done;
+        asm volatile(
+            "{\n\t.reg .pred P;\n\tmbarrier.test_wait.parity.shared::cta.b64 P, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, P;\n\t}"
+            : "=r"(done)
+            : "r"(bar), "r"(parity)
+            : "memory");
+        if (done) return true;
+    }
+    return false;
+}
+
+// a wait on the MMA barrier: blocking polls up to the default bound, or
+// non-blocking ones up to a bound set by gdn_set_wait_limit
+__device__ __forceinline__ bool wait_mma(uint32_t bar, uint32_t parity, uint32_t limit) {
+    return limit == 0 ? wait_parity(bar, parity, kSpinLimit) : test_parity(bar, parity, limit);
 }
 
 __device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
@@ -380,6 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_chunked_kernel(const 
     const uint32_t bar = saddr(&ms.bar);
     uint32_t phase = 0;
     bool ok = true;
+    const uint32_t limit = p.wait_limit;                       // 0: the default bound
 
     // hi and lo images of 32 FP32 state values (kd0 .. kd0 + 31 of row v)
     auto put_images = [&](int v, int kd0, const float (&x)[32]) {
@@ -537,7 +560,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_chunked_kernel(const 
             gemm_split(tR, qH, qL, kC, kH, kL, kC, 64, kK, false);
             commit(bar);
         }
-        ok = !__syncthreads_or(!wait_parity(bar, phase));
+        ok = !__syncthreads_or(!wait_mma(bar, phase, limit));
         phase ^= 1;
         if (!ok) break;
         fence_after();
@@ -696,7 +719,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_chunked_kernel(const 
             commit(bar);
         }
         if (c0 + kC < L) load_chunk(c0 + kC);
-        ok = !__syncthreads_or(!wait_parity(bar, phase));
+        ok = !__syncthreads_or(!wait_mma(bar, phase, limit));
         phase ^= 1;
         if (!ok) break;
         fence_after();
@@ -784,8 +807,11 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_chunked_kernel(const 
         }
     }
     if (!ok) {
-        if (tid == 0 && p.status) atomicOr(p.status, GDN_FLAG_TIMEOUT);
-        wait_parity(bar, phase ^ 1u);                           // the MMAs still in flight, bounded
+        // the MMAs still in flight, with the default bound: tensor memory is
+        // released only once they have finished writing it (a drain that
+        // runs out is reported and the memory released regardless)
+        const bool drained = wait_parity(bar, phase ^ 1u, kSpinLimit);
+        if (tid == 0 && p.status) atomicOr(p.status, GDN_FLAG_TIMEOUT | (drained ? 0 : GDN_FLAG_DRAIN));
     }
     fence_before();
     __syncthreads();
@@ -813,7 +839,11 @@ cudaError_t launch(const Params& p, int64_t units, cudaStream_t stream) {
 
 namespace gdn_internal {
 
-cudaError_t launch_prefill_chunked(const Params& p, int64_t units, gdn_dtype state_dtype, cudaStream_t stream) {
+uint32_t g_wait_limit = 0;
+
+cudaError_t launch_prefill_chunked(const Params& p0, int64_t units, gdn_dtype state_dtype, cudaStream_t stream) {
+    Params p = p0;
+    p.wait_limit = __atomic_load_n(&g_wait_limit, __ATOMIC_RELAXED);
     switch (state_dtype) {
     case GDN_F32: return launch<float>(p, units, stream);
     case GDN_BF16: return launch<__nv_bfloat16>(p, units, stream);

@@ -1229,6 +1229,8 @@ const char* gdn_status_str(gdn_status status) {
     return "unknown status";
 }
 
+void gdn_set_wait_limit(uint32_t polls) { __atomic_store_n(&gdn_internal::g_wait_limit, polls, __ATOMIC_RELAXED); }
+
 int32_t gdn_version(void) { return GDNSPEC_VERSION; }
 
 }  // extern "C"

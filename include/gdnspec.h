@@ -82,7 +82,12 @@ typedef enum { GDN_F32 = 0, GDN_BF16 = 1, GDN_F16 = 2 } gdn_dtype;
 #define GDN_FLAG_TOKEN_ROW  8  /* a token row outside [0, num_tokens), or cu_seqlens[i] < 0 or
                                   cu_seqlens[i+1] > cu_seqlens[batch]: sequence skipped */
 #define GDN_FLAG_TIMEOUT    16 /* gdn_prefill_chunked only: a wait on the tensor cores ran past its
-                                  bound; that sequence's outputs and final state are incomplete */
+                                  bound (gdn_set_wait_limit); that sequence's outputs and final
+                                  state are incomplete */
+#define GDN_FLAG_DRAIN      32 /* gdn_prefill_chunked only: after such a timeout, the wait (with the
+                                  default bound) for the products still in flight ran out too; the
+                                  CTA released its tensor memory regardless, since holding it would
+                                  block every later kernel on that SM */
 
 /*
  * dims->split flag: each warp of the decode step owns 8 of a unit's 128 V
@@ -350,6 +355,18 @@ GDNSPEC_API gdn_status gdn_spec_decode_conv(
  * Host only; reads no device state.
  */
 GDNSPEC_API int32_t gdn_spec_decode_split(const gdn_dims* dims, gdn_dtype state_dtype);
+
+/*
+ * Bound on each wait of gdn_prefill_chunked for its tensor-core products:
+ * 0 (the default) waits with blocking polls of the completion barrier, 2^24
+ * of them (well over a second); a non-zero bound counts non-blocking polls
+ * instead, so that a small one runs out for certain.  A wait that runs out
+ * sets GDN_FLAG_TIMEOUT and the CTA stops after waiting, with the default
+ * bound, for the products still in flight.  Process-wide, read at every
+ * launch; meant for exercising that path in tests.  No counterpart on the
+ * report pages.
+ */
+GDNSPEC_API void gdn_set_wait_limit(uint32_t polls);
 
 /* Static English text for a status code (never NULL). */
 GDNSPEC_API const char* gdn_status_str(gdn_status status);

@@ -238,6 +238,30 @@ def test_input_extremes(entry):
     _check(entry, ext, *_run(entry, ext, reads, writes), writes)
 
 
+def test_wait_timeout_is_flagged_and_the_next_launch_is_clean():
+    """A wait bound of one poll runs out on the first tensor-core wait: the
+    call sets GDN_FLAG_TIMEOUT (and not GDN_FLAG_DRAIN: the products in flight
+    finish under the default bound before tensor memory is released); with
+    the default bound restored, the next launch matches the oracle."""
+    case = _case([100, 30], synth.F32, H_k=1, H_v=8, seed=61)
+    reads, writes = _slots(case, 8, zero_every=10 ** 6, skip_every=10 ** 6)
+    pool = make_pool(case, DEV, slots=sorted(s for s in set(reads.tolist()) | set(writes.tolist()) if s >= 0))
+    t = device_tensors(case, DEV)
+    out = torch.zeros(case.num_tokens, case.H_v, case.V, dtype=torch.bfloat16, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    args = (t["q"], t["k"], t["v"], t["a"], t["b"], t["z"], t["A_log"], t["dt_bias"], t["norm_w"], pool.clone(),
+            torch.from_numpy(reads).to(DEV), torch.from_numpy(writes).to(DEV), t["cu_seqlens"], out)
+    gdn.binding.set_wait_limit(1)
+    try:
+        gdn.gdn_prefill_chunked(*args, status=st)
+        torch.cuda.synchronize()
+    finally:
+        gdn.binding.set_wait_limit(0)
+    flags = int(st.item())
+    assert flags & gdn.binding.GDN_FLAG_TIMEOUT and not flags & gdn.binding.GDN_FLAG_DRAIN, flags
+    _check("chunked", case, *_run("chunked", case, reads, writes), writes)
+
+
 def test_zz_report_errors():
     """Prints the measured errors of every comparison above (run with -s)."""
     for name, entry, e_out, e_state in ERRORS:
