@@ -590,7 +590,7 @@ def build_sets(args, rank, dev):
             def call(handle, flags, v=v, out=out, c=c):
                 gdn.gdn_spec_decode_conv(v["x"], conv_w, conv_b, conv_pool, v["cin"], v["cout"], v["a"], v["b"],
                                          v["z"], A_log, dt_bias, norm_w, pool, v["idx"], v["acc"], v["cu"], out,
-                                         H_k=c.H_k, max_T=8, flags=flags & GDN_PRE_INDEX, stream=handle)
+                                         H_k=c.H_k, max_T=8, flags=flags, stream=handle)
             cs = dataclasses.replace(c, state_indices=tables[s])
             ci = dataclasses.replace(ci0, x=x, conv_in=cperm[2 * s * B:(2 * s + 1) * B],
                                      conv_out=cperm[(2 * s + 1) * B:(2 * s + 2) * B])
@@ -630,7 +630,7 @@ def run_gpu(args, rank, world, local_rank):
     torch.cuda.set_device(dev)
     name = args.workload
     kind = kind_of(name)
-    flags = args.flags if kind == "decode" else (args.flags & GDN_PRE_INDEX if kind == "conv" else 0)
+    flags = args.flags if kind != "prefill" else 0
     sets, pool, case0, n_sets, num_slots = build_sets(args, rank, dev)
     stream = torch.cuda.current_stream(dev)
     handle = stream.cuda_stream
@@ -705,7 +705,7 @@ def run_gpu(args, rank, world, local_rank):
 
     # --- the same back-to-back steps without the early reads (decode only) ---
     plain_ms = None
-    if kind == "decode" and flags != 0:
+    if kind != "prefill" and flags != 0:
         torch.cuda.synchronize()
         p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         p0.record(stream)
@@ -869,9 +869,9 @@ def main():
     ap.add_argument("--split", type=lambda x: int(x, 0), default=0,
                     help="decode workloads: dims.split (0 = the library's choice; 1, 2, 4, 8, 0x102, 0x104)")
     ap.add_argument("--flags", type=lambda x: int(x, 0), default=GDN_PRE_INDEX | GDN_PRE_TOKENS | GDN_PRE_STATE,
-                    help="decode workloads: dims.flags (default 7 = GDN_PRE_INDEX | GDN_PRE_TOKENS | GDN_PRE_STATE: "
-                         "the resident inputs and the rotating sets' disjoint slots are not written by the preceding "
-                         "step; the conv workload keeps the index bit)")
+                    help="decode and conv workloads: dims.flags (default 7 = GDN_PRE_INDEX | GDN_PRE_TOKENS | "
+                         "GDN_PRE_STATE: the resident inputs and the rotating sets' disjoint state and conv slots are "
+                         "not written by the preceding step)")
     ap.add_argument("--prefill-form", choices=("chunked", "recurrent"), default="chunked",
                     help="prefill workloads: gdn_prefill_chunked (tensor cores) or gdn_prefill (per token)")
     args = ap.parse_args()

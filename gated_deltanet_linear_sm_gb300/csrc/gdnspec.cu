@@ -624,9 +624,13 @@ gdn_spec_decode_kernel(const __grid_constant__ Params p) {
     // slots, the status word) comes after the wait; every exit waits first, so
     // that no successor is released before this grid's predecessor has
     // completed.
+    // (the fused convolution reads its history rows, conv slots, in the token
+    // prologue: it runs the prologue early only when both the token rows and
+    // the recurrent slots, state and conv, are declared)
     const bool pre_index = (p.flags & GDN_PRE_INDEX) != 0;
-    const bool pre_tokens = !CONV && pre_index && (p.flags & GDN_PRE_TOKENS) != 0;
-    const bool pre_state = !CONV && pre_index && (p.flags & GDN_PRE_STATE) != 0;
+    const bool pre_both = (p.flags & (GDN_PRE_TOKENS | GDN_PRE_STATE)) == (GDN_PRE_TOKENS | GDN_PRE_STATE);
+    const bool pre_tokens = pre_index && (CONV ? pre_both : (p.flags & GDN_PRE_TOKENS) != 0);
+    const bool pre_state = pre_index && (CONV ? pre_both : (p.flags & GDN_PRE_STATE) != 0);
     bool waited = false;
     auto dep_wait = [&]() {
         if (!waited) {
@@ -1128,7 +1132,7 @@ gdn_status gdn_spec_decode_conv(const void* x, const void* conv_weight, const vo
         static_cast<int64_t>(cdims->state_len) < cdims->width - 1 + static_cast<int64_t>(dims->spec_stride))
         return GDN_ERR_BAD_SHAPE;
     if (state_dtype != GDN_F32 && state_dtype != GDN_BF16 && state_dtype != GDN_F16) return GDN_ERR_UNSUPPORTED;
-    if (dims->split > 1 || (dims->flags & (GDN_PRE_TOKENS | GDN_PRE_STATE))) return GDN_ERR_UNSUPPORTED;
+    if (dims->split > 1) return GDN_ERR_UNSUPPORTED;
     if (dims->batch == 0) return GDN_OK;
     if (!state_indices || !num_accepted || !x || !conv_weight || !conv_pool || !conv_in || !conv_out)
         return GDN_ERR_NULL_ARG;

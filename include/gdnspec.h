@@ -124,8 +124,10 @@ typedef enum { GDN_F32 = 0, GDN_BF16 = 1, GDN_F16 = 2 } gdn_dtype;
  * preceding kernel is one of this library's decode launches, or a kernel that
  * does not use programmatic dependent launch, every kernel before it has
  * completed when the early reads happen.
- * gdn_spec_decode_conv accepts GDN_PRE_INDEX only (its conv history may be
- * the preceding step's output); the prefill entry points take no flags.
+ * For gdn_spec_decode_conv, GDN_PRE_STATE also covers the conv slots the call
+ * reads (its conv history), and the token prologue, which convolves that
+ * history, runs early only with both GDN_PRE_TOKENS and GDN_PRE_STATE set.
+ * The prefill entry points take no flags.
  */
 #define GDN_PRE_INDEX  0x1
 #define GDN_PRE_TOKENS 0x2

@@ -164,9 +164,7 @@ def test_conv_bad_pointers_rejected(lib):
     assert _call_conv(lib, _dims(), _cdims(), bias=0x1002) == 4   # bias not 8-byte aligned
     assert _call_conv(lib, _dims(split=2), _cdims()) == 3         # the fused path has no split
     assert _call_conv(lib, _dims(split=binding.GDN_SPLIT_NARROW | 2), _cdims()) == 3
-    # the conv history may be the preceding step's output: token inputs are never read early
-    assert _call_conv(lib, _dims(flags=binding.GDN_PRE_INDEX | binding.GDN_PRE_TOKENS), _cdims()) == 3
-    assert _call_conv(lib, _dims(flags=binding.GDN_PRE_INDEX | binding.GDN_PRE_STATE), _cdims()) == 3
+    assert _call_conv(lib, _dims(flags=8), _cdims()) == 2                 # an unknown flag bit
     assert _call_conv(lib, _dims(batch=0), _cdims(), ptr=0) == 0  # empty batch: nothing launched
     assert lib.gdn_spec_decode_conv(*([None] * 6), None, *([None] * 12), ctypes.byref(_dims()), 0.1, 1e-5, 0,
                                     None, None) == 1

@@ -43,7 +43,7 @@ class Step:
         self.conv_host = self.conv.view(torch.int16).cpu().numpy().view(np.uint16).copy()
         self.conv_before = self.conv_host.copy()
 
-    def run(self, conv_in=None, conv_out=None):
+    def run(self, conv_in=None, conv_out=None, flags=0):
         case, ci = self.case, self.ci
         conv_in = ci.conv_in if conv_in is None else conv_in
         conv_out = ci.conv_out if conv_out is None else conv_out
@@ -57,7 +57,7 @@ class Step:
             t_bf16(case.z, DEV), t(case.A_log), t_bf16(case.dt_bias, DEV), t_bf16(case.norm_w, DEV), self.pool,
             t(case.state_indices), t(case.num_accepted), t(case.cu_seqlens), self.out, H_k=case.H_k,
             spec_token_indx=t(case.spec_token_indx) if case.spec_token_indx is not None else None,
-            scale=case.scale, eps=case.eps, max_T=case.max_T, status=self.status)
+            scale=case.scale, eps=case.eps, max_T=case.max_T, flags=flags, status=self.status)
         torch.cuda.synchronize()
         self.ref = orc.spec_decode_conv(
             x=ci.x, conv_weight=ci.weight, conv_bias=ci.bias, conv_pool=self.conv_host, conv_in=conv_in,
@@ -113,6 +113,21 @@ def test_head_ratios(ratio):
     the cluster exchanges them); 1 and 3 convolve q / k in every CTA."""
     case = _case(batch=5, H_k=2, H_v=2 * ratio, seed=90 + ratio)
     Step(case, synth.conv_inputs(case, seed=14 + ratio)).run().check()
+
+
+@pytest.mark.parametrize("flags", [1, 3, 7])
+def test_early_read_flags(flags):
+    """The early-read flags (with 7 the conv history and the state tile are
+    read before the dependency wait) give the oracle's results and the same
+    bits as flags = 0."""
+    case = _case(batch=8, seed=95, extra_rows=5, pad_prob=0.1)
+    ci = synth.conv_inputs(case, seed=19)
+    base = Step(case, ci).run()
+    flagged = Step(case, ci).run(flags=flags).check()
+    assert torch.equal(base.out.view(torch.int16), flagged.out.view(torch.int16))
+    assert torch.equal(base.conv.view(torch.int16), flagged.conv.view(torch.int16))
+    dt = torch.int32 if case.state_dtype == synth.F32 else torch.int16
+    assert torch.equal(base.pool.view(dt), flagged.pool.view(dt))
 
 
 def test_zero_history_and_skipped_conv_writes():
