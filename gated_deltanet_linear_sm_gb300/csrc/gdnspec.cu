@@ -310,15 +310,63 @@ __device__ __forceinline__ void prologue_token(Smem& s, const Params& p, int h, 
     prologue_token_f<NCW>(s, p, h, t, r, lane, qv, kv, vv, zraw, ws);
 }
 
+// The state in this lane's block to slot ws (skip -1).  With a staging
+// buffer the warp writes its 128 x NCW block to shared memory (8 lanes of a
+// row group fill 8 consecutive 32 / 64-byte rows: no bank conflicts) and one
+// lane hands it to the tensor-memory-access unit, which writes the strided
+// block to the slot; the buffer is reused once that store has read it.
+// Without one, every lane stores its rows itself.
+template <typename StateT, int NCW>
+__device__ __forceinline__ void write_slot(const float (&S)[Lanes<NCW>::kRows][4], const Params& p, long long ws,
+                                           int h, int lane, int col0, int rank, StateT* stage) {
+    using L = Lanes<NCW>;
+    const int cgi = lane % L::kColGroups;
+    const int rg = lane / L::kColGroups;
+    if (ws >= p.num_slots) raise_flag(p, rank, GDN_FLAG_SLOT_RANGE);
+    if (ws >= 0 && ws < p.num_slots) {
+        if (stage != nullptr) {
+            if (lane == 0) tma_wait_read();
+            __syncwarp();
+#pragma unroll
+            for (int r = 0; r < L::kRows; ++r)
+                StateIO<StateT>::stage4(stage + (rg + L::kRowGroups * r) * NCW + 4 * cgi, S[r]);
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            if (lane == 0)
+                tma_store_box(&p.pool_map, stage, col0 - 4 * cgi, static_cast<int>((ws * p.H_v + h) * kK));
+        } else {
+            StateT* d = static_cast<StateT*>(p.pool) + (ws * p.H_v + h) * kTile + col0;
+#pragma unroll
+            for (int r = 0; r < L::kRows; ++r)
+                StateIO<StateT>::store4(d + static_cast<int64_t>(rg + L::kRowGroups * r) * kV, S[r]);
+        }
+    }
+}
+
 // One draft token for this lane's 16x4 block: both reductions, the delta rule,
 // the readout into s.o, the state update and (when s.ws[t] names a slot) the
-// slot write.
-template <typename StateT, int NCW = kColsPerWarp>
+// slot write.  With PIPE the state after token t - 1 is staged for its slot
+// write while token t's partial products are formed (both only read S), and
+// the state after token t is left for the next call (or write_slot after the
+// last token): one CTA per SM waits on nothing between the two.
+template <typename StateT, int NCW = kColsPerWarp, bool PIPE = false>
 __device__ __forceinline__ void token_step(float (&S)[Lanes<NCW>::kRows][4], Smem& s, const Params& p, int t,
                                            int h, int lane, int col0, int row0, int rank, StateT* stage) {
     using L = Lanes<NCW>;
     const int cgi = lane % L::kColGroups;
     const int rg = lane / L::kColGroups;
+    long long pws = -1;                  // PIPE: the previous token's slot, staged below
+    if constexpr (PIPE) {
+        if (t > 0) pws = s.ws[t - 1];
+        if (pws >= p.num_slots) {
+            raise_flag(p, rank, GDN_FLAG_SLOT_RANGE);
+            pws = -1;
+        }
+        if (pws >= 0) {
+            if (lane == 0) tma_wait_read();
+            __syncwarp();
+        }
+    }
     const int c_own = (lane >> 2) & 3; // after the reduce-scatter: my column ...
     const int d_own = (lane >> 4) & 1; // ... and which dot product (0: k, 1: q)
     const float decay = s.decay[t];
@@ -346,6 +394,22 @@ __device__ __forceinline__ void token_step(float (&S)[Lanes<NCW>::kRows][4], Sme
                 upk2(xk, x[c], x[c + 1]);
                 upk2(xq, x[4 + c], x[5 + c]);
             }
+        if constexpr (PIPE) {
+            if (pws >= 0) {
+#pragma unroll
+                for (int rr = 0; rr < 4; ++rr)
+                    StateIO<StateT>::stage4(stage + (rg + L::kRowGroups * (4 * r4 + rr)) * NCW + 4 * cgi,
+                                            S[4 * r4 + rr]);
+            }
+        }
+    }
+    if constexpr (PIPE) {
+        if (pws >= 0) {
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            if (lane == 0)
+                tma_store_box(&p.pool_map, stage, col0 - 4 * cgi, static_cast<int>((pws * p.H_v + h) * kK));
+        }
     }
     // reduce-scatter over the row groups on lane bits 4, 3, 2: afterwards the
     // lane holds the sum of value index 4 d + c = (lane >> 2) & 7 (d = 0: k,
@@ -403,32 +467,9 @@ __device__ __forceinline__ void token_step(float (&S)[Lanes<NCW>::kRows][4], Sme
             }
     }
 
-    // the state after token t goes to slot s.ws[t] (skip -1).  With a staging
-    // buffer the warp writes its 128 x 16 block to shared memory (8 lanes of a
-    // row group fill 8 consecutive 32 / 64-byte rows: no bank conflicts) and
-    // one lane hands it to the tensor-memory-access unit, which writes the
-    // strided block to the slot; the buffer is reused once that store has
-    // read it.  Without one, every lane stores its rows itself.
-    const long long ws = s.ws[t];
-    if (ws >= p.num_slots) raise_flag(p, rank, GDN_FLAG_SLOT_RANGE);
-    if (ws >= 0 && ws < p.num_slots) {
-        if (stage != nullptr) {
-            if (lane == 0) tma_wait_read();
-            __syncwarp();
-#pragma unroll
-            for (int r = 0; r < L::kRows; ++r)
-                StateIO<StateT>::stage4(stage + (rg + L::kRowGroups * r) * NCW + 4 * cgi, S[r]);
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            __syncwarp();
-            if (lane == 0)
-                tma_store_box(&p.pool_map, stage, col0 - 4 * cgi, static_cast<int>((ws * p.H_v + h) * kK));
-        } else {
-            StateT* d = static_cast<StateT*>(p.pool) + (ws * p.H_v + h) * kTile + col0;
-#pragma unroll
-            for (int r = 0; r < L::kRows; ++r)
-                StateIO<StateT>::store4(d + static_cast<int64_t>(rg + L::kRowGroups * r) * kV, S[r]);
-        }
-    }
+    // the state after token t goes to slot s.ws[t] (skip -1); with PIPE, during
+    // the next token
+    if constexpr (!PIPE) write_slot<StateT, NCW>(S, p, s.ws[t], h, lane, col0, rank, stage);
 }
 
 // Gated RMSNorm epilogue over tokens 0 .. n-1 in shared memory: out = o *
@@ -591,7 +632,7 @@ __device__ __forceinline__ void conv_token(const Params& p, int bos, int t, cons
 //
 // Grid: one CTA per (unit, column slice); SPLIT CTAs of a unit form one cluster.
 // Block: 128 / NCW / SPLIT warps, each owning NCW of the unit's 128 V columns.
-template <typename StateT, int SPLIT, bool CONV = false, int NCW = kColsPerWarp>
+template <typename StateT, int SPLIT, bool CONV = false, int NCW = kColsPerWarp, bool PIPE = false>
 __global__ void __launch_bounds__(Config<StateT, SPLIT, NCW>::kThreads, NCW == kColsPerWarp ? 2 * SPLIT : SPLIT)
 gdn_spec_decode_kernel(const __grid_constant__ Params p) {
     using C = Config<StateT, SPLIT, NCW>;
@@ -774,7 +815,8 @@ gdn_spec_decode_kernel(const __grid_constant__ Params p) {
     StateT* stage = reinterpret_cast<StateT*>(smem_raw + C::kStageOffset +
                                               ((128u - (smem_addr(smem_raw) & 127u)) & 127u)) +
                     warp * C::kStageElems;
-    for (int t = 0; t < q_len; ++t) token_step<StateT, NCW>(S, s, p, t, h, lane, col0, row0, rank, stage);
+    for (int t = 0; t < q_len; ++t) token_step<StateT, NCW, PIPE>(S, s, p, t, h, lane, col0, row0, rank, stage);
+    if constexpr (PIPE) write_slot<StateT, NCW>(S, p, s.ws[q_len - 1], h, lane, col0, rank, stage);
 
     // ---- gated RMSNorm epilogue ----
     __syncthreads();                                           // s.o of this CTA complete
@@ -847,10 +889,10 @@ __global__ void __launch_bounds__(256, 2) gdn_prefill_kernel(const Params p) {
 
 // ---- host side ----------------------------------------------------------------
 
-template <typename StateT, int SPLIT, bool CONV = false, int NCW = kColsPerWarp>
+template <typename StateT, int SPLIT, bool CONV = false, int NCW = kColsPerWarp, bool PIPE = false>
 cudaError_t launch(const Params& p, int64_t units, cudaStream_t stream) {
     using C = Config<StateT, SPLIT, NCW>;
-    auto kernel = gdn_spec_decode_kernel<StateT, SPLIT, CONV, NCW>;
+    auto kernel = gdn_spec_decode_kernel<StateT, SPLIT, CONV, NCW, PIPE>;
     if (C::kSmem > 48 * 1024) {
         // opt in to more than 48 KB of dynamic shared memory, once per device
         static bool done[64] = {false};
@@ -884,10 +926,27 @@ cudaError_t launch(const Params& p, int64_t units, cudaStream_t stream) {
     return cudaLaunchKernelEx(&cfg, kernel, p);
 }
 
+// Pipelined slot writes (token_step's PIPE) when every CTA of the launch has
+// an SM to itself: there a CTA's token chain is latency-bound and staging one
+// token's state while the next token's products form shortens it (BS=4 bf16
+// 7.78 -> 7.63 us, BS=8 8.93 -> 8.70 us); with two CTAs per SM the longer
+// live ranges cost more than the overlap saves (BS=32 28.89 -> 29.29 us), and
+// the narrow layout loses too (BS=4 fp32 9.41 -> 9.57 us).
+bool pipelined(int64_t ctas) {
+    static int sms[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+    if (sms[dev] == 0 && cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return false;
+    return ctas <= sms[dev];
+}
+
 template <typename StateT>
 cudaError_t launch_split(const Params& p, int64_t units, int split, cudaStream_t stream) {
     switch (split) {
-    case 1: return launch<StateT, 1>(p, units, stream);
+    case 1:
+        return pipelined(units) ? launch<StateT, 1, false, kColsPerWarp, true>(p, units, stream)
+                                : launch<StateT, 1>(p, units, stream);
     case 2: return launch<StateT, 2>(p, units, stream);
     case 4: return launch<StateT, 4>(p, units, stream);
     case GDN_SPLIT_NARROW | 2: return launch<StateT, 2, false, 8>(p, units, stream);
