@@ -56,7 +56,8 @@ struct Params {
 // Process-wide bound on the chunked prefill's tensor-core waits (0: the default).
 extern uint32_t g_wait_limit;
 
-// Launch the chunked prefill kernel: one CTA per (sequence, v-head) unit.
+// Launch the chunked prefill kernel: one CTA per (sequence, v-head) unit, or a
+// 2-CTA cluster per unit when the units are fewer than half the SMs.
 cudaError_t launch_prefill_chunked(const Params& p, int64_t units, gdn_dtype state_dtype, cudaStream_t stream);
 
 }  // namespace gdn_internal

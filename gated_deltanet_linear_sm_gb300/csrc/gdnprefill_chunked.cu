@@ -16,7 +16,7 @@
 // over the chunk: the same quantities in exact arithmetic.  All decay factors
 // are e^(non-positive), so nothing overflows however strong the decay.
 //
-// Kernel (one CTA of 8 warps per (sequence, v-head), one CTA per SM):
+// Kernel (one CTA of 8 warps per (sequence, v-head) unit, or two, one CTA per SM):
 //  * Products run on the tensor cores as 128-row tcgen05.mma (kind::f16: bf16
 //    operands, FP32 accumulators) issued by one thread, at FP32 accuracy: every
 //    operand x is carried as two bf16 terms, hi = bf16(x) and lo = bf16(x - hi)
@@ -35,12 +35,19 @@
 //    Per chunk it is rescaled by e^(G_last) (tcgen05.ld / st) and V'^T K~ is
 //    accumulated into it; its hi and lo bf16 images are the B operands of X
 //    and O for the next chunk.
-//  * The unit lower-triangular solve runs on CUDA cores in FP32, two threads
-//    per value column with the column in registers, right-looking so that
-//    each step is a batch of independent FMAs.
+//  * The unit lower-triangular solve runs on CUDA cores in FP32, two (or
+//    four) threads per value column with the column in registers,
+//    right-looking so that each step is a batch of independent FMAs.
+//  * With fewer (sequence, v-head) units than half the SMs, a unit's 128 value
+//    columns are split over a 2-CTA cluster (64 each): the recurrence of a
+//    value column involves no other column, and the RMSNorm's sums of squares
+//    are exchanged through distributed shared memory once per chunk.
 //  * Every wait on the tensor cores is bounded.  On a timeout the CTA sets
-//    GDN_FLAG_TIMEOUT, waits (bounded) for the MMAs in flight, releases its
-//    tensor memory and stops.
+//    GDN_FLAG_TIMEOUT, writes no final state, waits (bounded) for the MMAs in
+//    flight and releases its tensor memory; a lone CTA stops at once, a
+//    2-CTA unit runs its remaining chunks (their outputs are not valid) so
+//    that both CTAs meet at every cluster barrier.
+#include <cooperative_groups.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -50,6 +57,8 @@
 
 #include "gdn_internal.h"
 #include "gdnspec.h"
+
+namespace cg = cooperative_groups;
 
 namespace {
 
@@ -68,47 +77,61 @@ constexpr uint32_t kSpinLimit = 1u << 24;       // try_wait polls before giving 
 // a tile of R rows is stored in atom columns of 64 elements; element (r, c)
 // sits at (c / 64) * R * 128 + r * 128 + (((c % 64) / 8) ^ (r % 8)) * 16 + (c % 8) * 2.
 // Token tiles have 64 rows and carry hi in columns 0 .. K-1, lo in K .. 2K-1.
-// Regions are reused once the products that read them have completed:
-//   kTileK   [64 t][hi 128 | lo 128 kd]   K^        after phase 2: the FP32 gate w silu(z) [64 t][128 v]
+// A CTA owns VC of the unit's 128 value columns (128, or 64 with the unit
+// over a 2-CTA cluster).  Regions are reused once the products that read
+// them have completed:
+//   kTileK   [64 t][hi 128 | lo 128 kd]   K^        after phase 2: the FP32 gate w silu(z) [64 t][VC]
 //   kTileQ   [64 t][hi 128 | lo 128 kd]   Q^        after MMA 1: K~^T hi | lo  [128 kd][64 t] each
-//   kTileS   [128 v][128 kd]              S^T hi
-//   kTileS2  [128 v][128 kd]              S^T lo    after MMA 1: V'^T hi | lo  [128 v][64 t] each
+//   kTileS   [VC v][128 kd]               S^T hi
+//   kTileS2  [VC v][128 kd]               S^T lo    after MMA 1: V'^T hi | lo  [VC v][64 t] each
 //   kTileR   [64 t][hi 64 | lo 64 s]      R~
 // A 128-row MMA over a 64-row tile reads 8 KB past each atom column; every
 // such read stays inside the shared-memory block and lands in unread lanes.
-constexpr int kTileK = 0;
-constexpr int kTileQ = kTileK + 32768;
-constexpr int kTileS = kTileQ + 32768;
-constexpr int kTileS2 = kTileS + 32768;
-constexpr int kTileR = kTileS2 + 32768;
-constexpr int kTileKdHi = kTileQ, kTileKdLo = kTileQ + 16384;
-constexpr int kTileVHi = kTileS2, kTileVLo = kTileS2 + 16384;
-constexpr int kGate = kTileK;                   // FP32 [64 t][128 v], column v stored at v ^ (t % 32)
-constexpr int kA2Half = 36;                     // floats per parity half-row (32 used; the pad puts
-                                                // the two halves of a row on different banks)
-constexpr int kA2Row = 2 * kA2Half;
-constexpr int kA2 = kTileR + 16384;             // A     fp32 [64 s][2 parity][36 (t/2)]
-constexpr int kBStride = kC + 1;                // odd row pitch: column walks are conflict-free
-constexpr int kBT = kA2 + kC * kA2Row * 4;      // B^T   fp32 [128 v][65]
-constexpr int kStagePitch = kV / 4 + 1;         // uint2 per padded output-staging row (aliases B^T)
-static_assert(kC * kStagePitch * 8 <= kV * kBStride * 4, "staging fits the B^T region");
-constexpr int kZStride = kV / 4 + 1;            // uint2 per padded gate row
-constexpr int kZ = kBT + kV * kBStride * 4;     // raw z, bf16 quads [64 t][33]
-constexpr int kMisc = kZ + kC * kZStride * 8;
-static_assert(kTileR + 16384 + 8192 <= kMisc, "the R~ tile's unread rows stay inside the block");
+template <int VC>
+struct Layout {
+    static constexpr int kTPC = kThreads / VC;                 // solve threads per value column: 2 or 4
+    static constexpr int kRowsPT = kC / kTPC;                  // rows per solve thread: 32 or 16
+    static constexpr int kTileK = 0;
+    static constexpr int kTileQ = kTileK + 32768;
+    static constexpr int kTileS = kTileQ + 32768;
+    static constexpr int kImg = VC * kK * 2;                   // one state image
+    static constexpr int kTileS2 = kTileS + kImg;
+    static constexpr int kTileR = kTileS2 + kImg;
+    static constexpr int kTileKdHi = kTileQ, kTileKdLo = kTileQ + 16384;
+    static constexpr int kTileVHi = kTileS2, kTileVLo = kTileS2 + VC * kC * 2;
+    static constexpr int kGate = kTileK;                       // FP32 [64 t][VC], column v stored at v ^ (t % 32)
+    static constexpr int kA2Part = kRowsPT + 4;                // floats per residue part of an A row (the pad
+                                                               // puts the parts on different banks)
+    static constexpr int kA2Row = kTPC * kA2Part;
+    static constexpr int kA2 = kTileR + 16384;                 // A     fp32 [64 s][kTPC residue][kA2Part (t / kTPC)]
+    static constexpr int kBStride = kC + 1;                    // odd row pitch: column walks are conflict-free
+    static constexpr int kBT = kA2 + kC * kA2Row * 4;          // B^T   fp32 [VC v][65]
+    static constexpr int kStagePitch = VC / 4 + 1;             // uint2 per padded output-staging row (aliases B^T)
+    static constexpr int kZStride = VC / 4 + 1;                // uint2 per padded gate row
+    static constexpr int kZ = kBT + VC * kBStride * 4;         // raw z, bf16 quads [64 t][VC / 4 + 1]
+    static constexpr int kMisc = (kZ + kC * kZStride * 8 + 15) / 16 * 16;
+    static_assert(kC * kStagePitch * 8 <= VC * kBStride * 4, "staging fits the B^T region");
+    static_assert(kC * VC * 4 <= 32768, "the gate fits the K^ region");
+    static_assert(2 * VC * kC * 2 <= kImg, "V'^T hi and lo fit the S^T lo region");
+    static_assert(kTileR + 16384 + 8192 <= kMisc, "the R~ tile's unread rows stay inside the block");
+};
 
 struct Misc {
     unsigned long long bar;                     // MMA completion barrier
     uint32_t tmem;                              // tensor-memory base column
     float gamma;                                // e^(G_last) of the current chunk
     float g[kC], G[kC], beta[kC], eG[kC], kfac[kC];   // G 16-byte aligned (float4 reads)
-    float ssq[2][kC];                           // per-row sums of squares of the two column halves
-    float wn[kV];                               // norm_w
+    float ssq[2][kC];                           // per-row sums of squares of this CTA's two column halves
+    float ssq_cta[2][kC];                       // with a 2-CTA unit: this CTA's sums, read by its peer
+                                                // (indexed by chunk parity)
+    float wn[kV];                               // norm_w of this CTA's columns
     int row[kC];
+    unsigned long long drain;                   // completion of every MMA issued, after a timeout
 };
-static_assert(kMisc % 16 == 0 && offsetof(Misc, G) % 16 == 0, "float4 reads of G");
-constexpr int kSmemBytes = kMisc + static_cast<int>(sizeof(Misc)) + 1024;   // + base alignment slack
-static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+static_assert(offsetof(Misc, G) % 16 == 0, "float4 reads of G");
+template <int VC>
+constexpr int smem_bytes() { return Layout<VC>::kMisc + static_cast<int>(sizeof(Misc)) + 1024; }   // + alignment
+static_assert(smem_bytes<128>() <= 227 * 1024 && smem_bytes<64>() <= 227 * 1024, "shared memory budget");
 
 __device__ __forceinline__ uint32_t swz(int r, int c, int R) {
     return static_cast<uint32_t>((c >> 6) * R * 128 + r * 128 + ((((c & 63) >> 3) ^ (r & 7)) << 4) + (c & 7) * 2);
@@ -336,35 +359,47 @@ __device__ __forceinline__ float silu(float z) { return __fdividef(z, 1.0f + __e
 //   phase 2  row warps 0,1    A from P            row warps 4,5   R~ (hi | lo) from R
 //            row warps        B = beta (v - e^G X) and O <- e^G O (each half of v)
 //            warps 2,3,6,7    K~^T hi and lo, then the FP32 output gate w silu(z)
-//            all warps        S^T <- e^(G_last) S^T (their quadrant's state rows)
-//   phase 3  all warps        (I + A) V' = B: two threads per value column,
-//                             rows split by parity; V'^T hi and lo tiles
+//            state warps      S^T <- e^(G_last) S^T (their state rows)
+//   phase 3  all warps        (I + A) V' = B: 256 / VC threads per value column,
+//                             rows split by residue; V'^T hi and lo tiles
 //   MMA 2                     O += R~ V',  S^T += V'^T K~
 //   phase 4  row warps        the gated RMSNorm of the chunk's rows (each warp
-//                             half of the columns); state images rows 0..63
-//            warps 2,3,6,7    state images rows 64..127; then all warps store
-//                             the output rows
+//                             half of the columns; a 2-CTA unit adds its
+//                             peer's sums of squares); state images
+//            then all warps store the output rows
 //
-// The state lives transposed in tensor memory (lane v, column kd), so its
-// images, the K-major [v][kd] operands, are written row by row.
-template <typename StateT>
+// VC: value columns of this CTA.  128: one CTA per (prompt, v-head); the
+// state warps are all 8.  64: the unit's columns over a 2-CTA cluster (a
+// column's recurrence needs no other column; only the RMSNorm adds over
+// them); state rows v < 64 live in lanes 0-63, so the row warps are the state
+// warps.  The state lives transposed in tensor memory (lane v, column kd), so
+// its images, the K-major [v][kd] operands, are written row by row.
+template <typename StateT, int VC>
 __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_chunked_kernel(const Params p) {
+    using Lay = Layout<VC>;
+    constexpr int CL = kV / VC;                                 // CTAs per unit
+    constexpr int TPC = Lay::kTPC;
+    constexpr int RPT = Lay::kRowsPT;
+    constexpr int HC = VC / 2;                                  // columns per half
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char* sm = smem_raw + ((1024u - (saddr(smem_raw) & 1023u)) & 1023u);
-    Misc& ms = *reinterpret_cast<Misc*>(sm + kMisc);
-    float* A2 = reinterpret_cast<float*>(sm + kA2);
-    float* BT = reinterpret_cast<float*>(sm + kBT);
-    float* Gate = reinterpret_cast<float*>(sm + kGate);
-    uint2* Zq = reinterpret_cast<uint2*>(sm + kZ);
-    uint2* Stage = reinterpret_cast<uint2*>(sm + kBT);          // output rows, after the solve
+    Misc& ms = *reinterpret_cast<Misc*>(sm + Lay::kMisc);
+    float* A2 = reinterpret_cast<float*>(sm + Lay::kA2);
+    float* BT = reinterpret_cast<float*>(sm + Lay::kBT);
+    float* Gate = reinterpret_cast<float*>(sm + Lay::kGate);
+    uint2* Zq = reinterpret_cast<uint2*>(sm + Lay::kZ);
+    uint2* Stage = reinterpret_cast<uint2*>(sm + Lay::kBT);     // output rows, after the solve
     const uint32_t sbase = saddr(sm);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quad = warp & 3;                                  // TMEM lane quadrant of this warp
     const int half = warp >> 2;                                 // which half of the columns
     const bool row_warp = quad < 2;                             // reaches the token rows 0-63
+    const bool state_warp = quad * 32 < VC;                     // holds state rows v
     const uint32_t lanes = static_cast<uint32_t>(quad * 32) << 16;
     const int row = quad * 32 + lane;                           // this thread's TMEM lane
-    const int unit = static_cast<int>(blockIdx.x);
+    const int rank = CL > 1 ? static_cast<int>(blockIdx.x % CL) : 0;
+    const int unit = static_cast<int>(blockIdx.x / CL);
+    const int cb = rank * VC;                                   // this CTA's first value column
     const int i = unit / p.H_v;
     const int h = unit - i * p.H_v;
     const int kh = h / p.group;
@@ -374,13 +409,14 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_chunked_kernel(const 
     const int L = __ldg(p.cu + i + 1) - bos;
     const long long rs = __ldg(p.read_slots + i);
     const long long wsl = __ldg(p.write_slots + i);
+    // (every CTA of a unit takes the same exits)
     if (L <= 0) return;
     if (bos < 0 || bos + L > p.num_tokens) {
-        if (tid == 0 && p.status) atomicOr(p.status, GDN_FLAG_TOKEN_ROW);
+        if (tid == 0 && rank == 0 && p.status) atomicOr(p.status, GDN_FLAG_TOKEN_ROW);
         return;
     }
     if (rs >= p.num_slots || wsl >= p.num_slots) {
-        if (tid == 0 && p.status) atomicOr(p.status, GDN_FLAG_SLOT_RANGE);
+        if (tid == 0 && rank == 0 && p.status) atomicOr(p.status, GDN_FLAG_SLOT_RANGE);
         return;
     }
 
@@ -391,14 +427,15 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_chunked_kernel(const 
     }
     if (tid == 0) {
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(saddr(&ms.bar)));
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(saddr(&ms.drain)));
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (gated && tid < kV) ms.wn[tid] = __bfloat162float(p.norm_w[tid]);
+    if (gated && tid < VC) ms.wn[tid] = __bfloat162float(p.norm_w[cb + tid]);
     fence_before();
     __syncthreads();
     fence_after();
     const uint32_t tm = ms.tmem;
-    const uint32_t tP = tm, tR = tm + 64, tX = tm + 128, tO = tm + 256, tS = tm + 384;
+    const uint32_t tP = tm, tR = tm + 64, tX = tm + 128, tO = tm + 128 + VC, tS = tm + 384;
     const uint32_t bar = saddr(&ms.bar);
     uint32_t phase = 0;
     bool ok = true;
@@ -410,18 +447,18 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_chunked_kernel(const 
         for (int j = 0; j < 4; ++j) {
             uint4 hi, lo;
             split8(x + 8 * j, hi, lo);
-            *reinterpret_cast<uint4*>(sm + kTileS + swz_chunk(v, (kd0 >> 3) + j, 128)) = hi;
-            *reinterpret_cast<uint4*>(sm + kTileS2 + swz_chunk(v, (kd0 >> 3) + j, 128)) = lo;
+            *reinterpret_cast<uint4*>(sm + Lay::kTileS + swz_chunk(v, (kd0 >> 3) + j, VC)) = hi;
+            *reinterpret_cast<uint4*>(sm + Lay::kTileS2 + swz_chunk(v, (kd0 >> 3) + j, VC)) = lo;
         }
     };
 
     // ---- initial state: S^T (FP32) into TMEM lane v, its images into the S^T tiles.
     //      Thread (v, half) covers kd in [64 half, 64 half + 64); a warp reads 32
     //      consecutive v of one kd row per load. ----
-    {
-        const StateT* src =
-            rs >= 0 ? static_cast<const StateT*>(p.pool) + (rs * p.H_v + h) * static_cast<int64_t>(kK * kV) + row
-                    : nullptr;
+    if (state_warp) {
+        const StateT* src = rs >= 0 ? static_cast<const StateT*>(p.pool) +
+                                          (rs * p.H_v + h) * static_cast<int64_t>(kK * kV) + cb + row
+                                    : nullptr;
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
             const int kd0 = 64 * half + 32 * c;
@@ -433,13 +470,14 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_chunked_kernel(const 
         }
     }
 
-    // Raw inputs of a chunk, 8 tokens per warp: q, k, z rows as bf16 quads, v one
-    // element per lane per load (v = lane + 32 e, so that its transposed store
-    // into B^T hits 32 distinct banks), a / b in lanes 0-15.  The next chunk's
-    // loads are issued as soon as the current chunk's solve has finished, so
-    // their latency overlaps the epilogue.
+    // Raw inputs of a chunk, 8 tokens per warp: q, k rows as bf16 quads, z quads
+    // of this CTA's columns, v one element per lane per load (v = cb + lane +
+    // 32 e, so that its transposed store into B^T hits 32 distinct banks), a / b
+    // in lanes 0-15.  The next chunk's loads are issued as soon as the current
+    // chunk's solve has finished, so their latency overlaps the epilogue.
+    constexpr int VE = VC / 32;                                  // v elements per lane
     uint2 qraw[8], kraw[8], zraw[8];
-    __nv_bfloat16 vraw[8][4];
+    __nv_bfloat16 vraw[8][VE];
     float ab;                                                   // lane j: a of token j, lane 8 + j: its b
     auto load_chunk = [&](int cs) {
         const int nn = min(kC, L - cs);
@@ -448,14 +486,15 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_chunked_kernel(const 
             const int t = warp + 8 * j;
             qraw[j] = kraw[j] = zraw[j] = make_uint2(0, 0);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) vraw[j][e] = __float2bfloat16_rn(0.f);
+            for (int e = 0; e < VE; ++e) vraw[j][e] = __float2bfloat16_rn(0.f);
             if (t < nn) {
                 const int64_t r = bos + cs + t;
                 qraw[j] = __ldg(reinterpret_cast<const uint2*>(p.q + r * p.q_stride + kh * kK) + lane);
                 kraw[j] = __ldg(reinterpret_cast<const uint2*>(p.k + r * p.k_stride + kh * kK) + lane);
 #pragma unroll
-                for (int e = 0; e < 4; ++e) vraw[j][e] = p.v[r * p.v_stride + h * kV + lane + 32 * e];
-                if (gated) zraw[j] = __ldg(reinterpret_cast<const uint2*>(p.z + r * p.z_stride + h * kV) + lane);
+                for (int e = 0; e < VE; ++e) vraw[j][e] = p.v[r * p.v_stride + h * kV + cb + lane + 32 * e];
+                if (gated && lane < VC / 4)
+                    zraw[j] = __ldg(reinterpret_cast<const uint2*>(p.z + r * p.z_stride + h * kV + cb) + lane);
             }
         }
         ab = 0.f;
@@ -468,6 +507,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_chunked_kernel(const 
 
     for (int c0 = 0; c0 < L; c0 += kC) {
         const int n = min(kC, L - c0);
+        const int cpar = (c0 / kC) & 1;                          // chunk parity
 
         // ---- phase 1: per token (8 per warp) k^, q^ (hi | lo), v (B^T), raw z,
         //      gates, from the raw rows loaded while the previous chunk finished ----
@@ -510,7 +550,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_chunked_kernel(const 
                 float qv[4], kv[4];
                 unpack4(qraw[j], qv);
                 unpack4(kraw[j], kv);
-                if (gated) Zq[t * kZStride + lane] = zraw[j];    // the output gate's input, exact
+                if (gated && lane < VC / 4) Zq[t * Lay::kZStride + lane] = zraw[j];   // the gate's input, exact
                 const float rq = rsqrtf(sums[j] + kQkEps) * p.scale;
                 const float rk = rsqrtf(sums[8 + j] + kQkEps);
                 split2(kv[0] * rk, kv[1] * rk, khi.x, klo.x);
@@ -518,12 +558,12 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_chunked_kernel(const 
                 split2(qv[0] * rq, qv[1] * rq, qhi.x, qlo.x);
                 split2(qv[2] * rq, qv[3] * rq, qhi.y, qlo.y);
 #pragma unroll
-                for (int e = 0; e < 4; ++e) BT[(lane + 32 * e) * kBStride + t] = __bfloat162float(vraw[j][e]);
+                for (int e = 0; e < VE; ++e) BT[(lane + 32 * e) * Lay::kBStride + t] = __bfloat162float(vraw[j][e]);
             }
-            *reinterpret_cast<uint2*>(sm + kTileK + swz(t, lane * 4, kC)) = khi;
-            *reinterpret_cast<uint2*>(sm + kTileK + swz(t, kK + lane * 4, kC)) = klo;
-            *reinterpret_cast<uint2*>(sm + kTileQ + swz(t, lane * 4, kC)) = qhi;
-            *reinterpret_cast<uint2*>(sm + kTileQ + swz(t, kK + lane * 4, kC)) = qlo;
+            *reinterpret_cast<uint2*>(sm + Lay::kTileK + swz(t, lane * 4, kC)) = khi;
+            *reinterpret_cast<uint2*>(sm + Lay::kTileK + swz(t, kK + lane * 4, kC)) = klo;
+            *reinterpret_cast<uint2*>(sm + Lay::kTileQ + swz(t, lane * 4, kC)) = qhi;
+            *reinterpret_cast<uint2*>(sm + Lay::kTileQ + swz(t, kK + lane * 4, kC)) = qlo;
         }
         __syncthreads();
         if (warp == 0) {
@@ -552,17 +592,25 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_chunked_kernel(const 
         // ---- MMA 1: P = K^ K^^T, R = Q^ K^^T, X = K^ S, O = Q^ S (hi.hi + lo.hi +
         //      hi.lo each) ----
         if (tid == 0) {
-            const uint32_t kH = sbase + kTileK, kL = kH + 2 * kC * 128;     // K^ hi | lo atom columns
-            const uint32_t qH = sbase + kTileQ, qL = qH + 2 * kC * 128;
+            const uint32_t kH = sbase + Lay::kTileK, kL = kH + 2 * kC * 128;     // K^ hi | lo atom columns
+            const uint32_t qH = sbase + Lay::kTileQ, qL = qH + 2 * kC * 128;
+            const uint32_t sH = sbase + Lay::kTileS, sL = sbase + Lay::kTileS2;
             gemm_split(tP, kH, kL, kC, kH, kL, kC, 64, kK, false);
-            gemm_split(tX, kH, kL, kC, sbase + kTileS, sbase + kTileS2, 128, 128, kK, false);
-            gemm_split(tO, qH, qL, kC, sbase + kTileS, sbase + kTileS2, 128, 128, kK, false);
+            gemm_split(tX, kH, kL, kC, sH, sL, VC, VC, kK, false);
+            gemm_split(tO, qH, qL, kC, sH, sL, VC, VC, kK, false);
             gemm_split(tR, qH, qL, kC, kH, kL, kC, 64, kK, false);
             commit(bar);
         }
-        ok = !__syncthreads_or(!wait_mma(bar, phase, limit));
-        phase ^= 1;
-        if (!ok) break;
+        {
+            // a 2-CTA unit never leaves the loop early (its CTAs meet at a cluster
+            // barrier every chunk): a wait that runs out is recorded and the chunk
+            // goes on
+            const bool done = wait_mma(bar, phase, limit);
+            const bool late = __syncthreads_or(!done);
+            phase ^= 1;
+            if (late) ok = false;
+            if (CL == 1 && late) break;
+        }
         fence_after();
 
         // ---- phase 2 ----
@@ -571,10 +619,10 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_chunked_kernel(const 
             const float Gt = ms.G[t], bt = ms.beta[t], eG = ms.eG[t];
             const bool live = t < n;
             if (half == 0) {
-                // A (s < t) from P, stored as A2[s][t % 2][t / 2]; the decay
+                // A (s < t) from P, stored as A2[s][t % TPC][t / TPC]; the decay
                 // factors are formed before any store, so no shared load waits
                 // behind a store
-                float* dst = A2 + (t & 1) * kA2Half + (t >> 1);
+                float* dst = A2 + (t % TPC) * Lay::kA2Part + (t / TPC);
 #pragma unroll
                 for (int s0 = 0; s0 < kC; s0 += 32) {
                     float x[32], d[32];
@@ -583,7 +631,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_chunked_kernel(const 
 #pragma unroll
                     for (int u = 0; u < 32; ++u) {
                         const int s = s0 + u;
-                        dst[s * kA2Row] = (live && s < t) ? bt * d[u] * x[u] : 0.f;
+                        dst[s * Lay::kA2Row] = (live && s < t) ? bt * d[u] * x[u] : 0.f;
                     }
                 }
             } else {
@@ -602,20 +650,20 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_chunked_kernel(const 
                     for (int j = 0; j < 4; ++j) {
                         uint4 hi, lo;
                         split8(x + 8 * j, hi, lo);
-                        *reinterpret_cast<uint4*>(sm + kTileR + swz_chunk(t, (s0 >> 3) + j, kC)) = hi;
-                        *reinterpret_cast<uint4*>(sm + kTileR + swz_chunk(t, 8 + (s0 >> 3) + j, kC)) = lo;
+                        *reinterpret_cast<uint4*>(sm + Lay::kTileR + swz_chunk(t, (s0 >> 3) + j, kC)) = hi;
+                        *reinterpret_cast<uint4*>(sm + Lay::kTileR + swz_chunk(t, 8 + (s0 >> 3) + j, kC)) = lo;
                     }
                 }
             }
             // B = beta (v - e^(G_t) X) and O <- e^(G_t) O for this half of the value columns
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                const int v0 = 64 * half + 32 * c;
+            for (int c = 0; c < HC / 32; ++c) {
+                const int v0 = HC * half + 32 * c;
                 float x[32];
                 tm_ld32(tX + lanes + v0, x);
 #pragma unroll
                 for (int u = 0; u < 32; ++u) {
-                    float* bp = &BT[(v0 + u) * kBStride + t];
+                    float* bp = &BT[(v0 + u) * Lay::kBStride + t];
                     *bp = live ? bt * (*bp - eG * x[u]) : 0.f;
                 }
                 tm_ld32(tO + lanes + v0, x);
@@ -635,32 +683,33 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_chunked_kernel(const 
                 for (int u = 0; u < 8; ++u) {
                     const int t = 8 * j + u;
                     const float kv =
-                        __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(sm + kTileK + swz(t, kd, kC))) +
-                        __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(sm + kTileK + swz(t, kK + kd, kC)));
+                        __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(sm + Lay::kTileK + swz(t, kd, kC))) +
+                        __bfloat162float(
+                            *reinterpret_cast<const __nv_bfloat16*>(sm + Lay::kTileK + swz(t, kK + kd, kC)));
                     x[u] = kv * ms.kfac[t];
                 }
                 uint4 hi, lo;
                 split8(x, hi, lo);
-                *reinterpret_cast<uint4*>(sm + kTileKdHi + swz_chunk(kd, j, 128)) = hi;
-                *reinterpret_cast<uint4*>(sm + kTileKdLo + swz_chunk(kd, j, 128)) = lo;
+                *reinterpret_cast<uint4*>(sm + Lay::kTileKdHi + swz_chunk(kd, j, 128)) = hi;
+                *reinterpret_cast<uint4*>(sm + Lay::kTileKdLo + swz_chunk(kd, j, 128)) = lo;
             }
             // every K^ read above is done before the gate overwrites the region
             asm volatile("bar.sync 1, 128;" ::: "memory");
             if (gated) {
                 // the output gate w silu(z) in FP32, [t][v ^ (t % 32)]
-                for (int e = wt; e < kC * (kV / 4); e += 128) {
-                    const int t = e >> 5, q4 = e & 31;
+                for (int e = wt; e < kC * (VC / 4); e += 128) {
+                    const int t = e / (VC / 4), q4 = e % (VC / 4);
                     float zz[4];
-                    unpack4(Zq[t * kZStride + q4], zz);
+                    unpack4(Zq[t * Lay::kZStride + q4], zz);
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
                         const int v = 4 * q4 + c;
-                        Gate[t * kV + (v ^ (t & 31))] = ms.wn[v] * silu(zz[c]);
+                        Gate[t * VC + (v ^ (t & 31))] = ms.wn[v] * silu(zz[c]);
                     }
                 }
             }
         }
-        {
+        if (state_warp) {
             // S^T <- e^(G_last) S^T: lane v of this quadrant, this half of the kd columns
             const float gamma = ms.gamma;
 #pragma unroll
@@ -677,51 +726,55 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_chunked_kernel(const 
         __syncthreads();
         fence_after();
 
-        // ---- phase 3: (I + A) V' = B.  Thread pair (2 vc, 2 vc + 1) of a warp
-        //      solves value column vc; member r owns rows t = 2 i + r in x[i].
-        //      Right-looking: once x_s is final its owner broadcasts it and both
-        //      remove its part from their later rows (A2[s][.][i] is zero for
-        //      rows t <= s, so the float4 groups may start below s + 1). ----
+        // ---- phase 3: (I + A) V' = B.  TPC threads per value column vc; member r
+        //      owns rows t = TPC i + r in x[i].  Right-looking: once x_s is final
+        //      its owner broadcasts it and all remove its part from their later
+        //      rows (A2[s][.][i] is zero for rows t <= s, so the float4 groups
+        //      may start below). ----
         {
-            const int vc = warp * 16 + (lane >> 1), r = lane & 1;
-            float x[32];
+            const int vc = tid / TPC, r = tid % TPC;
+            float x[RPT];
 #pragma unroll
-            for (int i2 = 0; i2 < 32; ++i2) x[i2] = BT[vc * kBStride + 2 * i2 + r];
-            const float* arow = A2 + r * kA2Half;
+            for (int i2 = 0; i2 < RPT; ++i2) x[i2] = BT[vc * Lay::kBStride + TPC * i2 + r];
+            const float* arow = A2 + r * Lay::kA2Part;
 #pragma unroll
             for (int s = 0; s < kC - 1; ++s) {
-                const float mine = (r == (s & 1)) ? x[s >> 1] : 0.f;
-                const float nxs = -__shfl_sync(0xffffffffu, mine, (lane & ~1) | (s & 1));
+                const float mine = (r == (s % TPC)) ? x[s / TPC] : 0.f;
+                const float nxs = -__shfl_sync(0xffffffffu, mine, (lane & ~(TPC - 1)) | (s % TPC));
 #pragma unroll
-                for (int i4 = (s >> 3); i4 < 8; ++i4) {
-                    const float4 a4 = *reinterpret_cast<const float4*>(arow + s * kA2Row + 4 * i4);
+                for (int i4 = (s / (4 * TPC)); i4 < RPT / 4; ++i4) {
+                    const float4 a4 = *reinterpret_cast<const float4*>(arow + s * Lay::kA2Row + 4 * i4);
                     fma2(x[4 * i4 + 0], x[4 * i4 + 1], a4.x, a4.y, nxs);
                     fma2(x[4 * i4 + 2], x[4 * i4 + 3], a4.z, a4.w, nxs);
                 }
             }
-            // V'^T tile rows vc, hi and lo: this thread's tokens 2 i + r
+            // V'^T tile rows vc, hi and lo: this thread's tokens TPC i + r
 #pragma unroll
-            for (int i2 = 0; i2 < 32; ++i2) {
+            for (int i2 = 0; i2 < RPT; ++i2) {
                 const __nv_bfloat16 hi = __float2bfloat16_rn(x[i2]);
                 const __nv_bfloat16 lo = __float2bfloat16_rn(x[i2] - __bfloat162float(hi));
-                *reinterpret_cast<__nv_bfloat16*>(sm + kTileVHi + swz(vc, 2 * i2 + r, 128)) = hi;
-                *reinterpret_cast<__nv_bfloat16*>(sm + kTileVLo + swz(vc, 2 * i2 + r, 128)) = lo;
+                *reinterpret_cast<__nv_bfloat16*>(sm + Lay::kTileVHi + swz(vc, TPC * i2 + r, VC)) = hi;
+                *reinterpret_cast<__nv_bfloat16*>(sm + Lay::kTileVLo + swz(vc, TPC * i2 + r, VC)) = lo;
             }
         }
         sync_for_mma();
 
         // ---- MMA 2: O += R~ V',  S^T += V'^T K~; meanwhile the next chunk's loads ----
         if (tid == 0) {
-            const uint32_t rH = sbase + kTileR, rL = rH + kC * 128;          // R~ hi | lo atom columns
-            gemm_split(tO, rH, rL, kC, sbase + kTileVHi, sbase + kTileVLo, 128, 128, kC, true);
-            gemm_split(tS, sbase + kTileVHi, sbase + kTileVLo, 128, sbase + kTileKdHi, sbase + kTileKdLo, 128,
-                       128, kC, true);
+            const uint32_t rH = sbase + Lay::kTileR, rL = rH + kC * 128;     // R~ hi | lo atom columns
+            const uint32_t vH = sbase + Lay::kTileVHi, vL = sbase + Lay::kTileVLo;
+            gemm_split(tO, rH, rL, kC, vH, vL, VC, VC, kC, true);
+            gemm_split(tS, vH, vL, VC, sbase + Lay::kTileKdHi, sbase + Lay::kTileKdLo, 128, 128, kC, true);
             commit(bar);
         }
         if (c0 + kC < L) load_chunk(c0 + kC);
-        ok = !__syncthreads_or(!wait_mma(bar, phase, limit));
-        phase ^= 1;
-        if (!ok) break;
+        {
+            const bool done = wait_mma(bar, phase, limit);
+            const bool late = __syncthreads_or(!done);
+            phase ^= 1;
+            if (late) ok = false;
+            if (CL == 1 && late) break;
+        }
         fence_after();
 
         // ---- phase 4: outputs (rows t < 64 on the row warps; each warp half of
@@ -730,15 +783,15 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_chunked_kernel(const 
         if (row_warp && gated) {
             float ss = 0.f;
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
+            for (int c = 0; c < HC / 32; ++c) {
                 float x[32];
-                tm_ld32(tO + lanes + 64 * half + 32 * c, x);
+                tm_ld32(tO + lanes + HC * half + 32 * c, x);
 #pragma unroll
                 for (int u = 0; u < 32; ++u) ss = fmaf(x[u], x[u], ss);
             }
             ms.ssq[half][row] = ss;
         }
-        if (more && !row_warp) {
+        if (more && state_warp && !row_warp) {
             // images of rows v = 64..127 while the others wait for the norms
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
@@ -749,23 +802,34 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_chunked_kernel(const 
             }
         }
         __syncthreads();
+        if constexpr (CL > 1) {
+            // the other CTA's half of each token's sum of squares (distributed
+            // shared memory; the buffer alternates with the chunk parity, so the
+            // peer's next write to it comes after the next chunk's barrier)
+            if (gated && tid < kC) ms.ssq_cta[cpar][tid] = ms.ssq[0][tid] + ms.ssq[1][tid];
+            cg::cluster_group cl = cg::this_cluster();
+            cl.sync();
+            if (gated && tid < kC)
+                ms.ssq[0][tid] += *cl.map_shared_rank(&ms.ssq_cta[cpar][tid], rank ^ 1);
+            __syncthreads();
+        }
         if (row_warp) {
             // normalised, gated rows into the staging buffer (the B^T region,
             // free until the next chunk), then the images of rows v = 0..63
             const int t = row;
             const float rinv = gated ? rsqrtf((ms.ssq[0][t] + ms.ssq[1][t]) * (1.0f / kV) + p.eps) : 1.0f;
-            uint2* srow = Stage + t * kStagePitch + 16 * half;
+            uint2* srow = Stage + t * Lay::kStagePitch + (HC / 4) * half;
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
+            for (int c = 0; c < HC / 32; ++c) {
                 float x[32];
-                tm_ld32(tO + lanes + 64 * half + 32 * c, x);
+                tm_ld32(tO + lanes + HC * half + 32 * c, x);
 #pragma unroll
                 for (int j4 = 0; j4 < 8; ++j4) {
                     float y[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const int v = 64 * half + 32 * c + 4 * j4 + e;
-                        y[e] = gated ? x[4 * j4 + e] * rinv * Gate[t * kV + (v ^ (t & 31))] : x[4 * j4 + e];
+                        const int v = HC * half + 32 * c + 4 * j4 + e;
+                        y[e] = gated ? x[4 * j4 + e] * rinv * Gate[t * VC + (v ^ (t & 31))] : x[4 * j4 + e];
                     }
                     srow[8 * c + j4] = make_uint2(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]));
                 }
@@ -781,13 +845,13 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_chunked_kernel(const 
             }
         }
         __syncthreads();
-        // the chunk's output rows, one warp per 256-byte row segment
+        // the chunk's output rows, this CTA's columns
 #pragma unroll
-        for (int e = tid; e < kC * (kV / 4); e += kThreads) {
-            const int t = e >> 5, q4 = e & 31;
+        for (int e = tid; e < kC * (VC / 4); e += kThreads) {
+            const int t = e / (VC / 4), q4 = e % (VC / 4);
             if (t < n)
-                *reinterpret_cast<uint2*>(p.out + ms.row[t] * p.out_stride + h * kV + 4 * q4) =
-                    Stage[t * kStagePitch + q4];
+                *reinterpret_cast<uint2*>(p.out + ms.row[t] * p.out_stride + h * kV + cb + 4 * q4) =
+                    Stage[t * Lay::kStagePitch + q4];
         }
         fence_before();
         __syncthreads();
@@ -795,8 +859,9 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_chunked_kernel(const 
     }
 
     // ---- the final state to its slot (rounded once), then release TMEM ----
-    if (ok && wsl >= 0) {
-        StateT* dst = static_cast<StateT*>(p.pool) + (wsl * p.H_v + h) * static_cast<int64_t>(kK * kV) + row;
+    if (ok && wsl >= 0 && state_warp) {
+        StateT* dst =
+            static_cast<StateT*>(p.pool) + (wsl * p.H_v + h) * static_cast<int64_t>(kK * kV) + cb + row;
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
             const int kd0 = 64 * half + 32 * c;
@@ -807,35 +872,70 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_chunked_kernel(const 
         }
     }
     if (!ok) {
-        // the MMAs still in flight, with the default bound: tensor memory is
-        // released only once they have finished writing it (a drain that
-        // runs out is reported and the memory released regardless)
-        const bool drained = wait_parity(bar, phase ^ 1u, kSpinLimit);
+        // the MMAs still in flight, with the default bound: one more commit, on
+        // a barrier of its own, tracks every MMA the issuing thread has started,
+        // and tensor memory is released only once they have finished writing it
+        // (a drain that runs out is reported and the memory released regardless)
+        if (tid == 0) commit(saddr(&ms.drain));
+        const bool drained = wait_parity(saddr(&ms.drain), 0u, kSpinLimit);
         if (tid == 0 && p.status) atomicOr(p.status, GDN_FLAG_TIMEOUT | (drained ? 0 : GDN_FLAG_DRAIN));
     }
     fence_before();
     __syncthreads();
     fence_after();
     if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tm));
+    // a CTA's shared memory stays until its peer has read the last sums
+    if constexpr (CL > 1) cg::this_cluster().sync();
 }
 
-template <typename StateT>
+template <typename StateT, int VC>
 cudaError_t launch(const Params& p, int64_t units, cudaStream_t stream) {
+    auto kernel = gdn_prefill_chunked_kernel<StateT, VC>;
+    constexpr int kSmem = smem_bytes<VC>();
     static bool done[64] = {false};                             // smem opt-in, once per device
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64 || !done[dev]) {
-        e = cudaFuncSetAttribute(gdn_prefill_chunked_kernel<StateT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kSmemBytes);
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) done[dev] = true;
     }
-    gdn_prefill_chunked_kernel<StateT><<<static_cast<unsigned>(units), kThreads, kSmemBytes, stream>>>(p);
-    return cudaGetLastError();
+    constexpr int CL = kV / VC;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(units * CL), 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = kSmem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CL;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = CL > 1 ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, p);
+}
+
+// Units fewer than half the SMs: each unit's value columns over a 2-CTA
+// cluster, so that twice the SMs run the chunks; otherwise one CTA per unit.
+template <typename StateT>
+cudaError_t launch_any(const Params& p, int64_t units, cudaStream_t stream) {
+    static int sms[64] = {0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64 && sms[dev] == 0) {
+        e = cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+    }
+    const int n_sm = (dev >= 0 && dev < 64) ? sms[dev] : 0;
+    if (2 * units <= n_sm) return launch<StateT, 64>(p, units, stream);
+    return launch<StateT, 128>(p, units, stream);
 }
 
 }  // namespace
+
 
 namespace gdn_internal {
 
@@ -845,9 +945,9 @@ cudaError_t launch_prefill_chunked(const Params& p0, int64_t units, gdn_dtype st
     Params p = p0;
     p.wait_limit = __atomic_load_n(&g_wait_limit, __ATOMIC_RELAXED);
     switch (state_dtype) {
-    case GDN_F32: return launch<float>(p, units, stream);
-    case GDN_BF16: return launch<__nv_bfloat16>(p, units, stream);
-    default: return launch<__half>(p, units, stream);
+    case GDN_F32: return launch_any<float>(p, units, stream);
+    case GDN_BF16: return launch_any<__nv_bfloat16>(p, units, stream);
+    default: return launch_any<__half>(p, units, stream);
     }
 }
 

@@ -272,8 +272,11 @@ GDNSPEC_API gdn_status gdn_prefill(
  *
  * Arguments, layouts, the caller contract and the status bits are those of
  * gdn_prefill; in addition GDN_FLAG_TIMEOUT reports a tensor-core wait that
- * ran past its bound.  One CTA per (sequence, v-head) holding the whole
- * 512-column tensor memory of its SM; ~214 KiB of shared memory.
+ * ran past its bound.  One CTA per (sequence, v-head) unit, holding the
+ * whole 512-column tensor memory of its SM (~214 KiB of shared memory); with
+ * fewer units than half the device's SMs, two CTAs per unit as a cluster,
+ * each with 64 of the value columns (~164 KiB of shared memory each).  The
+ * results do not depend on which form runs beyond FP32 rounding order.
  * Asynchronous on `stream`, allocates nothing.
  */
 GDNSPEC_API gdn_status gdn_prefill_chunked(
@@ -363,8 +366,9 @@ GDNSPEC_API int32_t gdn_spec_decode_split(const gdn_dims* dims, gdn_dtype state_
  * 0 (the default) waits with blocking polls of the completion barrier, 2^24
  * of them (well over a second); a non-zero bound counts non-blocking polls
  * instead, so that a small one runs out for certain.  A wait that runs out
- * sets GDN_FLAG_TIMEOUT and the CTA stops after waiting, with the default
- * bound, for the products still in flight.  Process-wide, read at every
+ * sets GDN_FLAG_TIMEOUT; the unit writes no final state and its CTAs end
+ * after waiting, with the default bound, for the products still in flight
+ * (a 2-CTA unit first runs its remaining chunks, whose outputs are invalid).  Process-wide, read at every
  * launch; meant for exercising that path in tests.  No counterpart on the
  * report pages.
  */

@@ -111,6 +111,16 @@ def test_ragged_lengths_and_padding(cuda_device, sd, split):
     _full_check(case, cuda_device, split)
 
 
+@pytest.mark.parametrize("sd", [synth.F32, synth.BF16, synth.F16])
+def test_ragged_padding_pipelined_writes(cuda_device, sd):
+    """At most one CTA per SM (8 sequences x 16 v-heads) the slot writes are
+    pipelined (a token's state is written during the next token): ragged
+    q_len in {0..8}, 30% padded slots (skipped writes, padded sequences)."""
+    case = synth.make_case(batch=8, H_k=2, H_v=16, T=8, state_dtype=sd, num_slots=128,
+                           q_lens="ragged", pad_prob=0.3, seed=34)
+    _full_check(case, cuda_device, 1)
+
+
 @pytest.mark.parametrize("split", SPLITS)
 def test_ungated_raw_readout(cuda_device, split):
     """z = norm_w = NULL: out is the raw readout o, which the RMSNorm would

@@ -113,6 +113,17 @@ def test_ragged_prompts(entry, sd):
     _check(entry, case, *_run(entry, case, reads, writes), writes)
 
 
+@pytest.mark.parametrize("sd", [synth.F32, synth.BF16, synth.F16])
+@pytest.mark.parametrize("entry", list(ENTRIES))
+def test_ragged_prompts_few_units(entry, sd):
+    """The same prompt lengths over 64 (sequence, v-head) units, fewer than
+    half the SMs: the chunked form splits each unit's value columns over a
+    2-CTA cluster (the test above, with 128 units, runs one CTA per unit)."""
+    case = _case([1, 7, 9, 63, 64, 65, 130, 200], sd, H_k=1, H_v=8, seed=62)
+    reads, writes = _slots(case, 9)
+    _check(entry, case, *_run(entry, case, reads, writes), writes)
+
+
 @pytest.mark.parametrize("sd", [synth.F32, synth.BF16])
 @pytest.mark.parametrize("entry", list(ENTRIES))
 def test_long_prompts_weak_decay(entry, sd):
@@ -238,12 +249,15 @@ def test_input_extremes(entry):
     _check(entry, ext, *_run(entry, ext, reads, writes), writes)
 
 
-def test_wait_timeout_is_flagged_and_the_next_launch_is_clean():
+@pytest.mark.parametrize("lens", [[100, 30], [100, 30] * 5], ids=["2-cta-units", "1-cta-units"])
+def test_wait_timeout_is_flagged_and_the_next_launch_is_clean(lens):
     """A wait bound of one poll runs out on the first tensor-core wait: the
     call sets GDN_FLAG_TIMEOUT (and not GDN_FLAG_DRAIN: the products in flight
     finish under the default bound before tensor memory is released); with
-    the default bound restored, the next launch matches the oracle."""
-    case = _case([100, 30], synth.F32, H_k=1, H_v=8, seed=61)
+    the default bound restored, the next launch matches the oracle.  16 units
+    run as 2-CTA clusters (which go on to the last chunk), 80 units as one
+    CTA each (which stop at once)."""
+    case = _case(lens, synth.F32, H_k=1, H_v=8, seed=61)
     reads, writes = _slots(case, 8, zero_every=10 ** 6, skip_every=10 ** 6)
     pool = make_pool(case, DEV, slots=sorted(s for s in set(reads.tolist()) | set(writes.tolist()) if s >= 0))
     t = device_tensors(case, DEV)
