@@ -5,11 +5,10 @@
 //
 // Chunked form (C = 64 tokens; S the K x V state at the chunk start; G_t the
 // running sum of the log-decays g inside the chunk; k^, q^ normalised rows):
-//   X = K^ S,  Y = Q^ S                                        (C x V)
 //   A_ts = beta_t e^(G_t - G_s) (k^_t . k^_s)   for s < t       (C x C)
-//   B_t  = beta_t (v_t - e^(G_t) X_t)
-//   (I + A) V' = B                                  (forward substitution)
-//   O_t  = e^(G_t) Y_t + sum_{s<=t} e^(G_t - G_s) (q^_t . k^_s) V'_s
+//   B_t  = beta_t (v_t - e^(G_t) S^T k^_t)
+//   V'   = (I + A)^-1 B
+//   o_t  = e^(G_t) S^T q^_t + sum_{s<=t} e^(G_t - G_s) (q^_t . k^_s) v'_s
 //   S   <- e^(G_last) S + K~^T V',   K~_s = e^(G_last - G_s) k^_s
 // This is the token recurrence S_t = e^(g_t) S_{t-1} + k^_t v'_t^T with
 // v'_t = beta_t (v_t - (e^(g_t) S_{t-1})^T k^_t) and o_t = S_t^T q^_t, unrolled
@@ -21,23 +20,23 @@
 //    operands, FP32 accumulators) issued by one thread, at FP32 accuracy: every
 //    operand x is carried as two bf16 terms, hi = bf16(x) and lo = bf16(x - hi)
 //    (|x - hi - lo| <= 2^-18 |x|), and a product accumulates the hi.hi, lo.hi
-//    and hi.lo terms in FP32 (the lo.lo term is below 2^-18).  A token operand
-//    (64 rows) stores hi and lo side by side along K, so the tensor cores add
-//    the terms inside the accumulator: its products land in lanes 0-63, and
-//    lanes 64-127 (the MMA's rows past the tile) are never read.  Operands are
-//    128-byte-swizzled K-major tiles in shared memory; accumulators live in
-//    tensor memory:
-//      columns   0- 63 P = K^ K^^T         columns  64-127 R = Q^ K^^T
-//      columns 128-255 X = K^ S            columns 256-383 O = Q^ S, then
-//                                          e^G O + R~ V' (the chunk's output)
-//      columns 384-511 S^T (FP32, carried over the whole prompt)
-//  * The FP32 state stays in tensor memory from the first chunk to the last.
-//    Per chunk it is rescaled by e^(G_last) (tcgen05.ld / st) and V'^T K~ is
-//    accumulated into it; its hi and lo bf16 images are the B operands of X
-//    and O for the next chunk.
-//  * The unit lower-triangular solve runs on CUDA cores in FP32, two (or
-//    four) threads per value column with the column in registers,
-//    right-looking so that each step is a batch of independent FMAs.
+//    and hi.lo terms in FP32 (the lo.lo term is below 2^-18).  Token tiles store
+//    hi and lo side by side along K, so the tensor cores add the terms inside
+//    the accumulator.
+//  * The value column v is the row (tensor-memory lane) of every product that
+//    involves the state: X^T = S^T K^^T, Y^T = S^T Q^^T, V'^T = B^T T^T (with
+//    T = (I + A)^-1), S^T += V'^T K~ and O^T += V'^T R~^T.  Their 128 rows are
+//    all live, and the per-column work after each product (B, the rescales,
+//    the images) is spread over the four lane quadrants, that is over all four
+//    SM sub-partitions.  The two token products P = K^ K^^T and R = Q^ K^^T
+//    form one 128-row product [K^; Q^] K^^T: lanes 0-63 hold P, lanes 64-127 R.
+//    Tensor-memory columns:
+//      0- 63 [P; R]     64-127 X^T     128-191 Y^T, then O^T     192-255 V'^T
+//      256-383 S^T (FP32, carried over the whole prompt)
+//  * T = (I + A)^-1 is formed on CUDA cores in FP32 by blocks: the four 16 x 16
+//    diagonal blocks by substitution, one thread per column, then the
+//    off-diagonal blocks by doubling (T_10 = -T_11 A_10 T_00 at 16 and then at
+//    32 rows), each a small dense product spread over the threads.
 //  * With fewer (sequence, v-head) units than half the SMs, a unit's 128 value
 //    columns are split over a 2-CTA cluster (64 each): the recurrence of a
 //    value column involves no other column, and the RMSNorm's sums of squares
@@ -76,59 +75,61 @@ constexpr uint32_t kSpinLimit = 1u << 24;       // try_wait polls before giving 
 // 128-byte-swizzled K-major bf16 tiles (the canonical SWIZZLE_128B layout):
 // a tile of R rows is stored in atom columns of 64 elements; element (r, c)
 // sits at (c / 64) * R * 128 + r * 128 + (((c % 64) / 8) ^ (r % 8)) * 16 + (c % 8) * 2.
-// Token tiles have 64 rows and carry hi in columns 0 .. K-1, lo in K .. 2K-1.
-// A CTA owns VC of the unit's 128 value columns (128, or 64 with the unit
-// over a 2-CTA cluster).  Regions are reused once the products that read
-// them have completed:
-//   kTileK   [64 t][hi 128 | lo 128 kd]   K^        after phase 2: the FP32 gate w silu(z) [64 t][VC]
-//   kTileQ   [64 t][hi 128 | lo 128 kd]   Q^        after MMA 1: K~^T hi | lo  [128 kd][64 t] each
-//   kTileS   [VC v][128 kd]               S^T hi
-//   kTileS2  [VC v][128 kd]               S^T lo    after MMA 1: V'^T hi | lo  [VC v][64 t] each
-//   kTileR   [64 t][hi 64 | lo 64 s]      R~
-// A 128-row MMA over a 64-row tile reads 8 KB past each atom column; every
-// such read stays inside the shared-memory block and lands in unread lanes.
+// A CTA owns VC of the unit's 128 value columns (128, or 64 with the unit over
+// a 2-CTA cluster).  Regions are reused once the products that read them have
+// completed:
+//   region 1  S^T hi | lo   [VC v][128 kd] each         (read by the first products)
+//             then B^T hi | lo [VC v][64 s] at its start, V'^T hi | lo in their place,
+//             and K~^T hi | lo [128 kd][64 t] in its second half
+//   region 2  [K^; Q^]      [128 rows][hi 128 | lo 128 kd]
+//             then the chunk's outputs, FP32 [64 t][VC + 4]
+//   kVT       v^T FP32 [VC v][65], then T FP32 [64][68] and T hi | lo [64 t][64 s]
+//   kA        A^T FP32 [64 s][68 t]
+//   kRt       R~ [64 t][hi 64 | lo 64 s]
+//   kM        FP32 products of the doubling steps (2 x [16][16], then [32][32])
+//   kZ        raw z, bf16 quads [64 t][VC / 4 + 1]
+// A 128-row product over a 64-row A tile (VC = 64) reads 8 KB past each atom
+// column; every such read stays inside region 1 and lands in unread lanes.
 template <int VC>
 struct Layout {
-    static constexpr int kTPC = kThreads / VC;                 // solve threads per value column: 2 or 4
-    static constexpr int kRowsPT = kC / kTPC;                  // rows per solve thread: 32 or 16
-    static constexpr int kTileK = 0;
-    static constexpr int kTileQ = kTileK + 32768;
-    static constexpr int kTileS = kTileQ + 32768;
     static constexpr int kImg = VC * kK * 2;                   // one state image
-    static constexpr int kTileS2 = kTileS + kImg;
-    static constexpr int kTileR = kTileS2 + kImg;
-    static constexpr int kTileKdHi = kTileQ, kTileKdLo = kTileQ + 16384;
-    static constexpr int kTileVHi = kTileS2, kTileVLo = kTileS2 + VC * kC * 2;
-    static constexpr int kGate = kTileK;                       // FP32 [64 t][VC], column v stored at v ^ (t % 32)
-    static constexpr int kA2Part = kRowsPT + 4;                // floats per residue part of an A row (the pad
-                                                               // puts the parts on different banks)
-    static constexpr int kA2Row = kTPC * kA2Part;
-    static constexpr int kA2 = kTileR + 16384;                 // A     fp32 [64 s][kTPC residue][kA2Part (t / kTPC)]
-    static constexpr int kBStride = kC + 1;                    // odd row pitch: column walks are conflict-free
-    static constexpr int kBT = kA2 + kC * kA2Row * 4;          // B^T   fp32 [VC v][65]
-    static constexpr int kStagePitch = VC / 4 + 1;             // uint2 per padded output-staging row (aliases B^T)
-    static constexpr int kZStride = VC / 4 + 1;                // uint2 per padded gate row
-    static constexpr int kZ = kBT + VC * kBStride * 4;         // raw z, bf16 quads [64 t][VC / 4 + 1]
+    static constexpr int kSHi = 0, kSLo = kImg;
+    static constexpr int kBHi = 0, kBLo = VC * 128;            // B^T, then V'^T: one atom column each
+    static constexpr int kKtHi = 32768, kKtLo = 49152;         // K~^T
+    static constexpr int kKQ = 65536;                          // [K^; Q^], atom columns of 16 KB
+    static constexpr int kKQLo = kKQ + 32768;                  // its lo half (columns 128-255)
+    static constexpr int kStage = kKQ;
+    static constexpr int kStagePitch = VC + 4;
+    static constexpr int kVT = 131072;
+    static constexpr int kVTPitch = kC + 1;                    // odd pitch: column walks are conflict-free
+    static constexpr int kT = kVT;
+    static constexpr int kTPitch = 68;
+    static constexpr int kTHi = kVT + 17408, kTLo = kTHi + 8192;
+    static constexpr int kA = kVT + 33792;
+    static constexpr int kAPitch = 68;
+    static constexpr int kRt = kA + 17408;
+    static constexpr int kM = kRt + 16384;
+    static constexpr int kZ = kM + 4096;
+    static constexpr int kZStride = VC / 4 + 1;                // uint2 per padded z row
     static constexpr int kMisc = (kZ + kC * kZStride * 8 + 15) / 16 * 16;
-    static_assert(kC * kStagePitch * 8 <= VC * kBStride * 4, "staging fits the B^T region");
-    static_assert(kC * VC * 4 <= 32768, "the gate fits the K^ region");
-    static_assert(2 * VC * kC * 2 <= kImg, "V'^T hi and lo fit the S^T lo region");
-    static_assert(kTileR + 16384 + 8192 <= kMisc, "the R~ tile's unread rows stay inside the block");
+    static_assert(2 * kImg <= 65536 && kKtHi >= 2 * VC * 128, "region 1");
+    static_assert(kC * kStagePitch * 4 <= 65536, "the output rows fit region 2");
+    static_assert(VC * kVTPitch * 4 <= 33792 && kTLo + 8192 <= kVT + 33792, "v^T and T share a region");
+    static_assert(64 * kTPitch * 4 <= 17408 && kTHi % 1024 == 0, "T");
+    static_assert(kRt % 1024 == 0, "R~ tile alignment");
 };
 
 struct Misc {
-    unsigned long long bar;                     // MMA completion barrier
-    uint32_t tmem;                              // tensor-memory base column
-    float gamma;                                // e^(G_last) of the current chunk
-    float g[kC], G[kC], beta[kC], eG[kC], kfac[kC];   // G 16-byte aligned (float4 reads)
-    float ssq[2][kC];                           // per-row sums of squares of this CTA's two column halves
-    float ssq_cta[2][kC];                       // with a 2-CTA unit: this CTA's sums, read by its peer
-                                                // (indexed by chunk parity)
+    float G[kC], g[kC], beta[kC], eG[kC], kfac[kC];            // G 16-byte aligned (float4 reads)
+    float ssq_cta[2][kC];                       // with a 2-CTA unit: this CTA's sums of squares, read
+                                                // by its peer (indexed by chunk parity)
     float wn[kV];                               // norm_w of this CTA's columns
     int row[kC];
+    unsigned long long bar;                     // MMA completion barrier
     unsigned long long drain;                   // completion of every MMA issued, after a timeout
+    uint32_t tmem;                              // tensor-memory base column
+    float gamma;                                // e^(G_last) of the current chunk
 };
-static_assert(offsetof(Misc, G) % 16 == 0, "float4 reads of G");
 template <int VC>
 constexpr int smem_bytes() { return Layout<VC>::kMisc + static_cast<int>(sizeof(Misc)) + 1024; }   // + alignment
 static_assert(smem_bytes<128>() <= 227 * 1024 && smem_bytes<64>() <= 227 * 1024, "shared memory budget");
@@ -333,70 +334,63 @@ __device__ __forceinline__ void load_decays(const float* G, float Gt, float (&d)
     }
 }
 
-// (x0, x1) <- (a0, a1) * c + (x0, x1), one paired FP32 FMA (each lane an
-// ordinary round-to-nearest FMA)
-__device__ __forceinline__ void fma2(float& x0, float& x1, float a0, float a1, float c) {
-    uint64_t xv = (static_cast<uint64_t>(__float_as_uint(x1)) << 32) | __float_as_uint(x0);
-    const uint64_t av = (static_cast<uint64_t>(__float_as_uint(a1)) << 32) | __float_as_uint(a0);
-    const uint64_t cv = (static_cast<uint64_t>(__float_as_uint(c)) << 32) | __float_as_uint(c);
-    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(xv) : "l"(av), "l"(cv));
-    x0 = __uint_as_float(static_cast<uint32_t>(xv));
-    x1 = __uint_as_float(static_cast<uint32_t>(xv >> 32));
-}
-
 // silu(z) = z sigmoid(z); for very negative z the denominator overflows and
 // the fast division returns zero
 __device__ __forceinline__ float silu(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
 
+// C[r][c0 .. c0+3] = sum_{q < Q} X(r, q) Y[q][c0 .. c0+3]: X read one element at
+// a time through xat(q), Y a row-major FP32 block read as float4
+template <int Q, typename XAt>
+__device__ __forceinline__ float4 rowdot4(XAt xat, const float* y, int y_pitch) {
+    float4 c = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int q = 0; q < Q; ++q) {
+        const float x = xat(q);
+        const float4 b = *reinterpret_cast<const float4*>(y + q * y_pitch);
+        c.x = fmaf(x, b.x, c.x);
+        c.y = fmaf(x, b.y, c.y);
+        c.z = fmaf(x, b.z, c.z);
+        c.w = fmaf(x, b.w, c.w);
+    }
+    return c;
+}
+
 // ---- the kernel -------------------------------------------------------------------------
 //
-// Per chunk, with the warps' TMEM quadrants q = warp % 4 (tcgen05.ld / st reach
-// only lanes 32q .. 32q + 31: token rows 0-63 of P, R, X and O from warps 0, 1,
-// 4, 5, the "row warps"; state rows v from the warps of their quadrant):
-//   phase 1  all warps        k^, q^ (hi | lo), v, z, gates of the chunk's 64
-//                             tokens; the running sum G
-//   MMA 1                     P = K^ K^^T, R = Q^ K^^T, X = K^ S, O = Q^ S
-//   phase 2  row warps 0,1    A from P            row warps 4,5   R~ (hi | lo) from R
-//            row warps        B = beta (v - e^G X) and O <- e^G O (each half of v)
-//            warps 2,3,6,7    K~^T hi and lo, then the FP32 output gate w silu(z)
-//            state warps      S^T <- e^(G_last) S^T (their state rows)
-//   phase 3  all warps        (I + A) V' = B: 256 / VC threads per value column,
-//                             rows split by residue; V'^T hi and lo tiles
-//   MMA 2                     O += R~ V',  S^T += V'^T K~
-//   phase 4  row warps        the gated RMSNorm of the chunk's rows (each warp
-//                             half of the columns; a 2-CTA unit adds its
-//                             peer's sums of squares); state images
-//            then all warps store the output rows
-//
-// VC: value columns of this CTA.  128: one CTA per (prompt, v-head); the
-// state warps are all 8.  64: the unit's columns over a 2-CTA cluster (a
-// column's recurrence needs no other column; only the RMSNorm adds over
-// them); state rows v < 64 live in lanes 0-63, so the row warps are the state
-// warps.  The state lives transposed in tensor memory (lane v, column kd), so
-// its images, the K-major [v][kd] operands, are written row by row.
+// Per chunk (quadrant q = warp % 4 reaches TMEM lanes 32q .. 32q + 31; the two
+// warps of a quadrant, hh = warp / 4, split the columns of each row; "column
+// lanes" are the lanes v < VC):
+//   phase 1  all warps      k^, q^ (hi | lo) into [K^; Q^], v^T, raw z, gates
+//   MMA 1                   [P; R] = [K^; Q^] K^^T,  X^T = S^T K^^T,  Y^T = S^T Q^^T
+//                           (meanwhile warp 0: the running sum G and its exponentials)
+//   phase 2  lanes 0-63     A^T from P              lanes 64-127   R~ (hi | lo) from R
+//            column lanes   B^T (hi | lo) = beta (v^T - e^G X^T);  O^T = e^G Y^T;  S^T <- e^(G_last) S^T
+//   phase 3  T = (I + A)^-1 by blocks; K~^T (hi | lo) meanwhile; T (hi | lo)
+//   MMA 2                   V'^T = B^T T^T
+//   phase 4  column lanes   V'^T (hi | lo)
+//   MMA 3                   S^T += V'^T K~,  O^T += V'^T R~^T  (meanwhile the next chunk's loads)
+//   phase 5  column lanes   O^T into the output rows (FP32); the state images
+//            all warps      the gated RMSNorm of 8 rows each, the rows to memory
 template <typename StateT, int VC>
 __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_chunked_kernel(const Params p) {
     using Lay = Layout<VC>;
     constexpr int CL = kV / VC;                                 // CTAs per unit
-    constexpr int TPC = Lay::kTPC;
-    constexpr int RPT = Lay::kRowsPT;
-    constexpr int HC = VC / 2;                                  // columns per half
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char* sm = smem_raw + ((1024u - (saddr(smem_raw) & 1023u)) & 1023u);
     Misc& ms = *reinterpret_cast<Misc*>(sm + Lay::kMisc);
-    float* A2 = reinterpret_cast<float*>(sm + Lay::kA2);
-    float* BT = reinterpret_cast<float*>(sm + Lay::kBT);
-    float* Gate = reinterpret_cast<float*>(sm + Lay::kGate);
+    float* VT = reinterpret_cast<float*>(sm + Lay::kVT);
+    float* Tm = reinterpret_cast<float*>(sm + Lay::kT);
+    float* At = reinterpret_cast<float*>(sm + Lay::kA);
+    float* Mb = reinterpret_cast<float*>(sm + Lay::kM);
+    float* Stage = reinterpret_cast<float*>(sm + Lay::kStage);
     uint2* Zq = reinterpret_cast<uint2*>(sm + Lay::kZ);
-    uint2* Stage = reinterpret_cast<uint2*>(sm + Lay::kBT);     // output rows, after the solve
     const uint32_t sbase = saddr(sm);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quad = warp & 3;                                  // TMEM lane quadrant of this warp
-    const int half = warp >> 2;                                 // which half of the columns
-    const bool row_warp = quad < 2;                             // reaches the token rows 0-63
-    const bool state_warp = quad * 32 < VC;                     // holds state rows v
+    const int hh = warp >> 2;                                   // which half of a row's columns
     const uint32_t lanes = static_cast<uint32_t>(quad * 32) << 16;
     const int row = quad * 32 + lane;                           // this thread's TMEM lane
+    const bool col_lane = quad * 32 < VC;                       // lane v holds value column v
     const int rank = CL > 1 ? static_cast<int>(blockIdx.x % CL) : 0;
     const int unit = static_cast<int>(blockIdx.x / CL);
     const int cb = rank * VC;                                   // this CTA's first value column
@@ -420,7 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_chunked_kernel(const 
         return;
     }
 
-    // ---- set-up: all 512 TMEM columns, the MMA barrier, the norm weight ----
+    // ---- set-up: all 512 TMEM columns, the barriers, the norm weight ----
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(saddr(&ms.tmem)));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
@@ -435,7 +429,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_chunked_kernel(const 
     __syncthreads();
     fence_after();
     const uint32_t tm = ms.tmem;
-    const uint32_t tP = tm, tR = tm + 64, tX = tm + 128, tO = tm + 128 + VC, tS = tm + 384;
+    const uint32_t tPR = tm, tX = tm + 64, tO = tm + 128, tVp = tm + 192, tS = tm + 256;
     const uint32_t bar = saddr(&ms.bar);
     uint32_t phase = 0;
     bool ok = true;
@@ -447,21 +441,42 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_chunked_kernel(const 
         for (int j = 0; j < 4; ++j) {
             uint4 hi, lo;
             split8(x + 8 * j, hi, lo);
-            *reinterpret_cast<uint4*>(sm + Lay::kTileS + swz_chunk(v, (kd0 >> 3) + j, VC)) = hi;
-            *reinterpret_cast<uint4*>(sm + Lay::kTileS2 + swz_chunk(v, (kd0 >> 3) + j, VC)) = lo;
+            *reinterpret_cast<uint4*>(sm + Lay::kSHi + swz_chunk(v, (kd0 >> 3) + j, VC)) = hi;
+            *reinterpret_cast<uint4*>(sm + Lay::kSLo + swz_chunk(v, (kd0 >> 3) + j, VC)) = lo;
         }
     };
+    // 32 FP32 values of a [rows][64] operand row r, columns c0 .. c0 + 31, as
+    // its hi and lo tiles
+    auto put_row64 = [&](uint32_t hi_off, uint32_t lo_off, int r, int rows, int c0, const float (&x)[32]) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            uint4 hi, lo;
+            split8(x + 8 * j, hi, lo);
+            *reinterpret_cast<uint4*>(sm + hi_off + swz_chunk(r, (c0 >> 3) + j, rows)) = hi;
+            *reinterpret_cast<uint4*>(sm + lo_off + swz_chunk(r, (c0 >> 3) + j, rows)) = lo;
+        }
+    };
+    // bounded wait on the MMA barrier; a lone CTA stops at a timeout, a 2-CTA
+    // unit records it and goes on (its CTAs meet at a cluster barrier every chunk)
+    auto wait_products = [&]() -> bool {
+        const bool done = wait_mma(bar, phase, limit);
+        const bool late = __syncthreads_or(!done);
+        phase ^= 1;
+        if (late) ok = false;
+        fence_after();
+        return CL == 1 && late;
+    };
 
-    // ---- initial state: S^T (FP32) into TMEM lane v, its images into the S^T tiles.
-    //      Thread (v, half) covers kd in [64 half, 64 half + 64); a warp reads 32
+    // ---- initial state: S^T (FP32) into TMEM lane v, its images into region 1.
+    //      Thread (v, hh) covers kd in [64 hh, 64 hh + 64); a warp reads 32
     //      consecutive v of one kd row per load. ----
-    if (state_warp) {
+    if (col_lane) {
         const StateT* src = rs >= 0 ? static_cast<const StateT*>(p.pool) +
                                           (rs * p.H_v + h) * static_cast<int64_t>(kK * kV) + cb + row
                                     : nullptr;
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
-            const int kd0 = 64 * half + 32 * c;
+            const int kd0 = 64 * hh + 32 * c;
             float x[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) x[j] = src ? load_elem(src + (kd0 + j) * kV) : 0.f;
@@ -472,13 +487,14 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_chunked_kernel(const 
 
     // Raw inputs of a chunk, 8 tokens per warp: q, k rows as bf16 quads, z quads
     // of this CTA's columns, v one element per lane per load (v = cb + lane +
-    // 32 e, so that its transposed store into B^T hits 32 distinct banks), a / b
-    // in lanes 0-15.  The next chunk's loads are issued as soon as the current
-    // chunk's solve has finished, so their latency overlaps the epilogue.
+    // 32 e, so that its transposed store hits 32 distinct banks), a / b bits in
+    // lanes 0-15 (converted only in phase 1, so that nothing waits on the loads
+    // before then).  The next chunk's loads are issued while the last products
+    // of the current one run.
     constexpr int VE = VC / 32;                                  // v elements per lane
     uint2 qraw[8], kraw[8], zraw[8];
     __nv_bfloat16 vraw[8][VE];
-    float ab;                                                   // lane j: a of token j, lane 8 + j: its b
+    unsigned short ab_raw;                                      // lane j: a of token j, lane 8 + j: its b
     auto load_chunk = [&](int cs) {
         const int nn = min(kC, L - cs);
 #pragma unroll
@@ -497,10 +513,10 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_chunked_kernel(const 
                     zraw[j] = __ldg(reinterpret_cast<const uint2*>(p.z + r * p.z_stride + h * kV + cb) + lane);
             }
         }
-        ab = 0.f;
+        ab_raw = 0;
         if (lane < 16 && warp + 8 * (lane & 7) < nn) {
             const int64_t r = bos + cs + warp + 8 * (lane & 7);
-            ab = __bfloat162float(lane < 8 ? p.a[r * p.a_stride + h] : p.b[r * p.b_stride + h]);
+            ab_raw = __bfloat16_as_ushort(lane < 8 ? p.a[r * p.a_stride + h] : p.b[r * p.b_stride + h]);
         }
     };
     load_chunk(0);
@@ -508,11 +524,12 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_chunked_kernel(const 
     for (int c0 = 0; c0 < L; c0 += kC) {
         const int n = min(kC, L - c0);
         const int cpar = (c0 / kC) & 1;                          // chunk parity
+        const bool more = c0 + kC < L;
 
-        // ---- phase 1: per token (8 per warp) k^, q^ (hi | lo), v (B^T), raw z,
-        //      gates, from the raw rows loaded while the previous chunk finished ----
+        // ---- phase 1: per token (8 per warp) k^ and q^ (hi | lo) into [K^; Q^],
+        //      v into v^T, raw z, gates ----
         {
-            // gates of the warp's 8 tokens, one per lane
+            const float ab = __uint_as_float(static_cast<uint32_t>(ab_raw) << 16);
             const float b_in = __shfl_down_sync(0xffffffffu, ab, 8);
             const int t = warp + 8 * lane;
             if (lane < 8) {
@@ -528,46 +545,59 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_chunked_kernel(const 
                 ms.beta[t] = beta;
             }
         }
-        // squared norms of the 8 q and 8 k rows, reduced together
-        float sums[16];
+        {
+            // squared norms of the 8 q and 8 k rows, reduced together
+            float sums[16];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            float qv[4], kv[4];
-            unpack4(qraw[j], qv);
-            unpack4(kraw[j], kv);
-            sums[j] = qv[0] * qv[0] + qv[1] * qv[1] + qv[2] * qv[2] + qv[3] * qv[3];
-            sums[8 + j] = kv[0] * kv[0] + kv[1] * kv[1] + kv[2] * kv[2] + kv[3] * kv[3];
-        }
-#pragma unroll
-        for (int m = 16; m >= 1; m >>= 1)
-#pragma unroll
-            for (int j = 0; j < 16; ++j) sums[j] += __shfl_xor_sync(0xffffffffu, sums[j], m);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const int t = warp + 8 * j;
-            uint2 khi = make_uint2(0, 0), klo = khi, qhi = khi, qlo = khi;
-            if (t < n) {
+            for (int j = 0; j < 8; ++j) {
                 float qv[4], kv[4];
                 unpack4(qraw[j], qv);
                 unpack4(kraw[j], kv);
-                if (gated && lane < VC / 4) Zq[t * Lay::kZStride + lane] = zraw[j];   // the gate's input, exact
-                const float rq = rsqrtf(sums[j] + kQkEps) * p.scale;
-                const float rk = rsqrtf(sums[8 + j] + kQkEps);
-                split2(kv[0] * rk, kv[1] * rk, khi.x, klo.x);
-                split2(kv[2] * rk, kv[3] * rk, khi.y, klo.y);
-                split2(qv[0] * rq, qv[1] * rq, qhi.x, qlo.x);
-                split2(qv[2] * rq, qv[3] * rq, qhi.y, qlo.y);
-#pragma unroll
-                for (int e = 0; e < VE; ++e) BT[(lane + 32 * e) * Lay::kBStride + t] = __bfloat162float(vraw[j][e]);
+                sums[j] = qv[0] * qv[0] + qv[1] * qv[1] + qv[2] * qv[2] + qv[3] * qv[3];
+                sums[8 + j] = kv[0] * kv[0] + kv[1] * kv[1] + kv[2] * kv[2] + kv[3] * kv[3];
             }
-            *reinterpret_cast<uint2*>(sm + Lay::kTileK + swz(t, lane * 4, kC)) = khi;
-            *reinterpret_cast<uint2*>(sm + Lay::kTileK + swz(t, kK + lane * 4, kC)) = klo;
-            *reinterpret_cast<uint2*>(sm + Lay::kTileQ + swz(t, lane * 4, kC)) = qhi;
-            *reinterpret_cast<uint2*>(sm + Lay::kTileQ + swz(t, kK + lane * 4, kC)) = qlo;
+#pragma unroll
+            for (int m = 16; m >= 1; m >>= 1)
+#pragma unroll
+                for (int j = 0; j < 16; ++j) sums[j] += __shfl_xor_sync(0xffffffffu, sums[j], m);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int t = warp + 8 * j;
+                uint2 khi = make_uint2(0, 0), klo = khi, qhi = khi, qlo = khi;
+                if (t < n) {
+                    float qv[4], kv[4];
+                    unpack4(qraw[j], qv);
+                    unpack4(kraw[j], kv);
+                    if (gated && lane < VC / 4) Zq[t * Lay::kZStride + lane] = zraw[j];   // the gate's input, exact
+                    const float rq = rsqrtf(sums[j] + kQkEps) * p.scale;
+                    const float rk = rsqrtf(sums[8 + j] + kQkEps);
+                    split2(kv[0] * rk, kv[1] * rk, khi.x, klo.x);
+                    split2(kv[2] * rk, kv[3] * rk, khi.y, klo.y);
+                    split2(qv[0] * rq, qv[1] * rq, qhi.x, qlo.x);
+                    split2(qv[2] * rq, qv[3] * rq, qhi.y, qlo.y);
+#pragma unroll
+                    for (int e = 0; e < VE; ++e) VT[(lane + 32 * e) * Lay::kVTPitch + t] = __bfloat162float(vraw[j][e]);
+                }
+                *reinterpret_cast<uint2*>(sm + Lay::kKQ + swz(t, lane * 4, 128)) = khi;
+                *reinterpret_cast<uint2*>(sm + Lay::kKQ + swz(t, kK + lane * 4, 128)) = klo;
+                *reinterpret_cast<uint2*>(sm + Lay::kKQ + swz(64 + t, lane * 4, 128)) = qhi;
+                *reinterpret_cast<uint2*>(sm + Lay::kKQ + swz(64 + t, kK + lane * 4, 128)) = qlo;
+            }
         }
-        __syncthreads();
+        sync_for_mma();
+
+        // ---- MMA 1: [P; R] = [K^; Q^] K^^T and [X^T | Y^T] = S^T [K^; Q^]^T
+        //      (hi.hi + lo.hi + hi.lo each) ----
+        if (tid == 0) {
+            const uint32_t kqH = sbase + Lay::kKQ, kqL = sbase + Lay::kKQLo;
+            const uint32_t sH = sbase + Lay::kSHi, sL = sbase + Lay::kSLo;
+            gemm_split(tPR, kqH, kqL, 128, kqH, kqL, 128, 64, kK, false);
+            gemm_split(tX, sH, sL, VC, kqH, kqL, 128, 128, kK, false);              // [X^T | Y^T]
+            commit(bar);
+        }
         if (warp == 0) {
-            // G = inclusive running sum of g; e^(G_t), e^(G_last - G_t), e^(G_last)
+            // while the products run: G = inclusive running sum of g; e^(G_t),
+            // e^(G_last - G_t), e^(G_last)
             const float g0 = ms.g[2 * lane], g1 = ms.g[2 * lane + 1];
             float s = g0 + g1;
 #pragma unroll
@@ -587,135 +617,98 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_chunked_kernel(const 
                 ms.kfac[t] = t < n ? expf(G_last - ms.G[t]) : 0.f;
             }
         }
-        sync_for_mma();
-
-        // ---- MMA 1: P = K^ K^^T, R = Q^ K^^T, X = K^ S, O = Q^ S (hi.hi + lo.hi +
-        //      hi.lo each) ----
-        if (tid == 0) {
-            const uint32_t kH = sbase + Lay::kTileK, kL = kH + 2 * kC * 128;     // K^ hi | lo atom columns
-            const uint32_t qH = sbase + Lay::kTileQ, qL = qH + 2 * kC * 128;
-            const uint32_t sH = sbase + Lay::kTileS, sL = sbase + Lay::kTileS2;
-            gemm_split(tP, kH, kL, kC, kH, kL, kC, 64, kK, false);
-            gemm_split(tX, kH, kL, kC, sH, sL, VC, VC, kK, false);
-            gemm_split(tO, qH, qL, kC, sH, sL, VC, VC, kK, false);
-            gemm_split(tR, qH, qL, kC, kH, kL, kC, 64, kK, false);
-            commit(bar);
-        }
-        {
-            // a 2-CTA unit never leaves the loop early (its CTAs meet at a cluster
-            // barrier every chunk): a wait that runs out is recorded and the chunk
-            // goes on
-            const bool done = wait_mma(bar, phase, limit);
-            const bool late = __syncthreads_or(!done);
-            phase ^= 1;
-            if (late) ok = false;
-            if (CL == 1 && late) break;
-        }
-        fence_after();
+        if (wait_products()) break;
 
         // ---- phase 2 ----
-        if (row_warp) {
-            const int t = row;                                  // token row of this lane
-            const float Gt = ms.G[t], bt = ms.beta[t], eG = ms.eG[t];
-            const bool live = t < n;
-            if (half == 0) {
-                // A (s < t) from P, stored as A2[s][t % TPC][t / TPC]; the decay
-                // factors are formed before any store, so no shared load waits
-                // behind a store
-                float* dst = A2 + (t % TPC) * Lay::kA2Part + (t / TPC);
+        {
+            // K~^T [kd][t] = k^_t[kd] e^(G_last - G_t) (k^ = hi + lo): thread
+            // (j = warp, kd4 = 4 lane) forms the 16-byte chunk j (8 tokens) of rows
+            // kd4 .. kd4 + 3, hi and lo
+            const int kd4 = 4 * lane, j = warp;
+            float x[4][8];
 #pragma unroll
-                for (int s0 = 0; s0 < kC; s0 += 32) {
-                    float x[32], d[32];
-                    load_decays(ms.G + s0, Gt, d);
-                    tm_ld32(tP + lanes + s0, x);
+            for (int u = 0; u < 8; ++u) {
+                const int t = 8 * j + u;
+                float hv[4], lv[4];
+                unpack4(*reinterpret_cast<const uint2*>(sm + Lay::kKQ + swz(t, kd4, 128)), hv);
+                unpack4(*reinterpret_cast<const uint2*>(sm + Lay::kKQ + swz(t, kK + kd4, 128)), lv);
+                const float f = ms.kfac[t];
 #pragma unroll
-                    for (int u = 0; u < 32; ++u) {
-                        const int s = s0 + u;
-                        dst[s * Lay::kA2Row] = (live && s < t) ? bt * d[u] * x[u] : 0.f;
-                    }
-                }
-            } else {
-                // R~ (s <= t) from R, hi | lo
-#pragma unroll
-                for (int s0 = 0; s0 < kC; s0 += 32) {
-                    float x[32], d[32];
-                    load_decays(ms.G + s0, Gt, d);
-                    tm_ld32(tR + lanes + s0, x);
-#pragma unroll
-                    for (int u = 0; u < 32; ++u) {
-                        const int s = s0 + u;
-                        x[u] = (live && s <= t) ? d[u] * x[u] : 0.f;
-                    }
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        uint4 hi, lo;
-                        split8(x + 8 * j, hi, lo);
-                        *reinterpret_cast<uint4*>(sm + Lay::kTileR + swz_chunk(t, (s0 >> 3) + j, kC)) = hi;
-                        *reinterpret_cast<uint4*>(sm + Lay::kTileR + swz_chunk(t, 8 + (s0 >> 3) + j, kC)) = lo;
-                    }
-                }
+                for (int c = 0; c < 4; ++c) x[c][u] = (hv[c] + lv[c]) * f;
             }
-            // B = beta (v - e^(G_t) X) and O <- e^(G_t) O for this half of the value columns
 #pragma unroll
-            for (int c = 0; c < HC / 32; ++c) {
-                const int v0 = HC * half + 32 * c;
-                float x[32];
-                tm_ld32(tX + lanes + v0, x);
+            for (int c = 0; c < 4; ++c) {
+                uint4 hi, lo;
+                split8(x[c], hi, lo);
+                *reinterpret_cast<uint4*>(sm + Lay::kKtHi + swz_chunk(kd4 + c, j, 128)) = hi;
+                *reinterpret_cast<uint4*>(sm + Lay::kKtLo + swz_chunk(kd4 + c, j, 128)) = lo;
+            }
+        }
+        {
+            // token rows of [P; R]: this warp's 32 columns s0 .. s0 + 31
+            const int t = row & 63;
+            const int s0 = 32 * hh;
+            const float Gt = ms.G[t];
+            const bool live = t < n;
+            float x[32], d[32];
+            load_decays(ms.G + s0, Gt, d);
+            tm_ld32(tPR + lanes + s0, x);
+            if (quad < 2) {
+                // A (s < t), stored transposed: A^T[s][t]
+                const float bt = ms.beta[t];
 #pragma unroll
                 for (int u = 0; u < 32; ++u) {
-                    float* bp = &BT[(v0 + u) * Lay::kBStride + t];
-                    *bp = live ? bt * (*bp - eG * x[u]) : 0.f;
+                    const int s = s0 + u;
+                    At[s * Lay::kAPitch + t] = (live && s < t) ? bt * d[u] * x[u] : 0.f;
                 }
-                tm_ld32(tO + lanes + v0, x);
+            } else {
+                // R~ (s <= t), hi | lo
 #pragma unroll
-                for (int u = 0; u < 32; ++u) x[u] *= eG;
-                tm_st32(tO + lanes + v0, x);
-            }
-        } else {
-            // K~^T [kd][t] = k^_t[kd] e^(G_last - G_t) (k^ = hi + lo), split again:
-            // one 16-byte chunk (8 tokens) of each part per item (the Q^ region,
-            // free since MMA 1)
-            const int wt = tid - 64 * (1 + half);              // 0..127 over warps 2, 3, 6, 7
-            for (int e = wt; e < kK * (kC / 8); e += 128) {
-                const int kd = e & (kK - 1), j = e >> 7;
-                float x[8];
+                for (int u = 0; u < 32; ++u) x[u] = (live && s0 + u <= t) ? d[u] * x[u] : 0.f;
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const int t = 8 * j + u;
-                    const float kv =
-                        __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(sm + Lay::kTileK + swz(t, kd, kC))) +
-                        __bfloat162float(
-                            *reinterpret_cast<const __nv_bfloat16*>(sm + Lay::kTileK + swz(t, kK + kd, kC)));
-                    x[u] = kv * ms.kfac[t];
-                }
-                uint4 hi, lo;
-                split8(x, hi, lo);
-                *reinterpret_cast<uint4*>(sm + Lay::kTileKdHi + swz_chunk(kd, j, 128)) = hi;
-                *reinterpret_cast<uint4*>(sm + Lay::kTileKdLo + swz_chunk(kd, j, 128)) = lo;
-            }
-            // every K^ read above is done before the gate overwrites the region
-            asm volatile("bar.sync 1, 128;" ::: "memory");
-            if (gated) {
-                // the output gate w silu(z) in FP32, [t][v ^ (t % 32)]
-                for (int e = wt; e < kC * (VC / 4); e += 128) {
-                    const int t = e / (VC / 4), q4 = e % (VC / 4);
-                    float zz[4];
-                    unpack4(Zq[t * Lay::kZStride + q4], zz);
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        const int v = 4 * q4 + c;
-                        Gate[t * VC + (v ^ (t & 31))] = ms.wn[v] * silu(zz[c]);
-                    }
+                for (int j = 0; j < 4; ++j) {
+                    uint4 hi, lo;
+                    split8(x + 8 * j, hi, lo);
+                    *reinterpret_cast<uint4*>(sm + Lay::kRt + swz_chunk(t, (s0 >> 3) + j, kC)) = hi;
+                    *reinterpret_cast<uint4*>(sm + Lay::kRt + swz_chunk(t, 8 + (s0 >> 3) + j, kC)) = lo;
                 }
             }
         }
-        if (state_warp) {
-            // S^T <- e^(G_last) S^T: lane v of this quadrant, this half of the kd columns
+        if (col_lane) {
+            // value column v = row: tokens t0 .. t0 + 31
+            const int v = row;
+            const int t0 = 32 * hh;
+            float x[32];
+            // B^T = beta (v^T - e^G X^T), hi | lo
+            tm_ld32(tX + lanes + t0, x);
+#pragma unroll
+            for (int u4 = 0; u4 < 8; ++u4) {
+                const float4 b4 = *reinterpret_cast<const float4*>(ms.beta + t0 + 4 * u4);
+                const float4 e4 = *reinterpret_cast<const float4*>(ms.eG + t0 + 4 * u4);
+                const float bb[4] = {b4.x, b4.y, b4.z, b4.w}, ee[4] = {e4.x, e4.y, e4.z, e4.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int u = 4 * u4 + e;
+                    x[u] = (t0 + u < n) ? bb[e] * (VT[v * Lay::kVTPitch + t0 + u] - ee[e] * x[u]) : 0.f;
+                }
+            }
+            put_row64(Lay::kBHi, Lay::kBLo, v, VC, t0, x);
+            // O^T <- e^G Y^T
+            tm_ld32(tO + lanes + t0, x);
+#pragma unroll
+            for (int u4 = 0; u4 < 8; ++u4) {
+                const float4 e4 = *reinterpret_cast<const float4*>(ms.eG + t0 + 4 * u4);
+                x[4 * u4] *= e4.x;
+                x[4 * u4 + 1] *= e4.y;
+                x[4 * u4 + 2] *= e4.z;
+                x[4 * u4 + 3] *= e4.w;
+            }
+            tm_st32(tO + lanes + t0, x);
+            // S^T <- e^(G_last) S^T, this half of the kd columns
             const float gamma = ms.gamma;
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
-                const uint32_t col = tS + lanes + 64 * half + 32 * c;
-                float x[32];
+                const uint32_t col = tS + lanes + 64 * hh + 32 * c;
                 tm_ld32(col, x);
 #pragma unroll
                 for (int u = 0; u < 32; ++u) x[u] *= gamma;
@@ -726,132 +719,240 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_chunked_kernel(const 
         __syncthreads();
         fence_after();
 
-        // ---- phase 3: (I + A) V' = B.  TPC threads per value column vc; member r
-        //      owns rows t = TPC i + r in x[i].  Right-looking: once x_s is final
-        //      its owner broadcasts it and all remove its part from their later
-        //      rows (A2[s][.][i] is zero for rows t <= s, so the float4 groups
-        //      may start below). ----
-        {
-            const int vc = tid / TPC, r = tid % TPC;
-            float x[RPT];
+        // ---- phase 3: T = (I + A)^-1.  (a) the diagonal 16 x 16 blocks, thread
+        //      (b, c) of warps 0-1 substituting column c of block b; meanwhile the
+        //      other warps zero T's upper blocks ----
+        if (tid < 64) {
+            const int b = tid >> 4, c = tid & 15;
+            float x[16];
 #pragma unroll
-            for (int i2 = 0; i2 < RPT; ++i2) x[i2] = BT[vc * Lay::kBStride + TPC * i2 + r];
-            const float* arow = A2 + r * Lay::kA2Part;
+            for (int r = 0; r < 16; ++r) x[r] = r == c ? 1.f : 0.f;
+            const float* arow = At + (16 * b) * Lay::kAPitch + 16 * b;
 #pragma unroll
-            for (int s = 0; s < kC - 1; ++s) {
-                const float mine = (r == (s % TPC)) ? x[s / TPC] : 0.f;
-                const float nxs = -__shfl_sync(0xffffffffu, mine, (lane & ~(TPC - 1)) | (s % TPC));
+            for (int k = 0; k < 15; ++k) {
+                // x_r -= A[r][k] x_k for r > k (A^T[k][r] is zero for r <= k)
+                const float nxk = -x[k];
 #pragma unroll
-                for (int i4 = (s / (4 * TPC)); i4 < RPT / 4; ++i4) {
-                    const float4 a4 = *reinterpret_cast<const float4*>(arow + s * Lay::kA2Row + 4 * i4);
-                    fma2(x[4 * i4 + 0], x[4 * i4 + 1], a4.x, a4.y, nxs);
-                    fma2(x[4 * i4 + 2], x[4 * i4 + 3], a4.z, a4.w, nxs);
+                for (int r4 = k / 4; r4 < 4; ++r4) {
+                    const float4 a4 = *reinterpret_cast<const float4*>(arow + k * Lay::kAPitch + 4 * r4);
+                    x[4 * r4 + 0] = fmaf(a4.x, nxk, x[4 * r4 + 0]);
+                    x[4 * r4 + 1] = fmaf(a4.y, nxk, x[4 * r4 + 1]);
+                    x[4 * r4 + 2] = fmaf(a4.z, nxk, x[4 * r4 + 2]);
+                    x[4 * r4 + 3] = fmaf(a4.w, nxk, x[4 * r4 + 3]);
                 }
             }
-            // V'^T tile rows vc, hi and lo: this thread's tokens TPC i + r
 #pragma unroll
-            for (int i2 = 0; i2 < RPT; ++i2) {
-                const __nv_bfloat16 hi = __float2bfloat16_rn(x[i2]);
-                const __nv_bfloat16 lo = __float2bfloat16_rn(x[i2] - __bfloat162float(hi));
-                *reinterpret_cast<__nv_bfloat16*>(sm + Lay::kTileVHi + swz(vc, TPC * i2 + r, VC)) = hi;
-                *reinterpret_cast<__nv_bfloat16*>(sm + Lay::kTileVLo + swz(vc, TPC * i2 + r, VC)) = lo;
-            }
-        }
-        sync_for_mma();
-
-        // ---- MMA 2: O += R~ V',  S^T += V'^T K~; meanwhile the next chunk's loads ----
-        if (tid == 0) {
-            const uint32_t rH = sbase + Lay::kTileR, rL = rH + kC * 128;     // R~ hi | lo atom columns
-            const uint32_t vH = sbase + Lay::kTileVHi, vL = sbase + Lay::kTileVLo;
-            gemm_split(tO, rH, rL, kC, vH, vL, VC, VC, kC, true);
-            gemm_split(tS, vH, vL, VC, sbase + Lay::kTileKdHi, sbase + Lay::kTileKdLo, 128, 128, kC, true);
-            commit(bar);
-        }
-        if (c0 + kC < L) load_chunk(c0 + kC);
-        {
-            const bool done = wait_mma(bar, phase, limit);
-            const bool late = __syncthreads_or(!done);
-            phase ^= 1;
-            if (late) ok = false;
-            if (CL == 1 && late) break;
-        }
-        fence_after();
-
-        // ---- phase 4: outputs (rows t < 64 on the row warps; each warp half of
-        //      the columns), then the state images for the next chunk ----
-        const bool more = c0 + kC < L;
-        if (row_warp && gated) {
-            float ss = 0.f;
-#pragma unroll
-            for (int c = 0; c < HC / 32; ++c) {
-                float x[32];
-                tm_ld32(tO + lanes + HC * half + 32 * c, x);
-#pragma unroll
-                for (int u = 0; u < 32; ++u) ss = fmaf(x[u], x[u], ss);
-            }
-            ms.ssq[half][row] = ss;
-        }
-        if (more && state_warp && !row_warp) {
-            // images of rows v = 64..127 while the others wait for the norms
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                const int kd0 = 64 * half + 32 * c;
-                float x[32];
-                tm_ld32(tS + lanes + kd0, x);
-                put_images(row, kd0, x);
+            for (int r = 0; r < 16; ++r) Tm[(16 * b + r) * Lay::kTPitch + 16 * b + c] = x[r];
+        } else {
+            const int w = tid - 64;                             // 0 .. 191
+            // the six 16 x 16 blocks above the diagonal
+            for (int e = w; e < 6 * 256; e += 192) {
+                const int blk = e >> 8, r = (e >> 4) & 15, c = e & 15;
+                const int bi = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
+                const int bj = blk < 3 ? 1 + blk : (blk < 5 ? blk - 1 : 3);
+                Tm[(16 * bi + r) * Lay::kTPitch + 16 * bj + c] = 0.f;
             }
         }
         __syncthreads();
-        if constexpr (CL > 1) {
-            // the other CTA's half of each token's sum of squares (distributed
-            // shared memory; the buffer alternates with the chunk parity, so the
-            // peer's next write to it comes after the next chunk's barrier)
-            if (gated && tid < kC) ms.ssq_cta[cpar][tid] = ms.ssq[0][tid] + ms.ssq[1][tid];
-            cg::cluster_group cl = cg::this_cluster();
-            cl.sync();
-            if (gated && tid < kC)
-                ms.ssq[0][tid] += *cl.map_shared_rank(&ms.ssq_cta[cpar][tid], rank ^ 1);
-            __syncthreads();
+        // (b) 16-row doubling: for J = 0, 1 (blocks b0 = 2J, b1 = 2J + 1)
+        //     M_J = A_{b1 b0} T_{b0 b0}, then T_{b1 b0} = -T_{b1 b1} M_J
+        if (tid < 128) {
+            const int J = tid >> 6, r = (tid >> 2) & 15, c4 = 4 * (tid & 3);
+            const int b0 = 16 * (2 * J), b1 = b0 + 16;
+            const float4 m = rowdot4<16>([&](int q) { return At[(b0 + q) * Lay::kAPitch + b1 + r]; },
+                                         Tm + b0 * Lay::kTPitch + b0 + c4, Lay::kTPitch);
+            *reinterpret_cast<float4*>(Mb + J * 256 + r * 16 + c4) = m;
         }
-        if (row_warp) {
-            // normalised, gated rows into the staging buffer (the B^T region,
-            // free until the next chunk), then the images of rows v = 0..63
-            const int t = row;
-            const float rinv = gated ? rsqrtf((ms.ssq[0][t] + ms.ssq[1][t]) * (1.0f / kV) + p.eps) : 1.0f;
-            uint2* srow = Stage + t * Lay::kStagePitch + (HC / 4) * half;
+        __syncthreads();
+        if (tid < 128) {
+            const int J = tid >> 6, r = (tid >> 2) & 15, c4 = 4 * (tid & 3);
+            const int b0 = 16 * (2 * J), b1 = b0 + 16;
+            const float4 m = rowdot4<16>([&](int q) { return Tm[(b1 + r) * Lay::kTPitch + b1 + q]; },
+                                         Mb + J * 256 + c4, 16);
+            *reinterpret_cast<float4*>(Tm + (b1 + r) * Lay::kTPitch + b0 + c4) = make_float4(-m.x, -m.y, -m.z, -m.w);
+        }
+        __syncthreads();
+        // (c) 32-row doubling: M = A[32..63][0..31] T[0..31][0..31], then
+        //     T[32..63][0..31] = -T[32..63][32..63] M.  Thread (r2, c4, hq): rows
+        //     2 r2 and 2 r2 + 1, columns c4 .. c4 + 3, over q in [16 hq, 16 hq + 16);
+        //     the two halves of q are added across neighbouring lanes.
+        {
+            const int hq = tid & 1, r2 = 2 * (tid >> 4), c4 = 4 * ((tid >> 1) & 7);
+            float acc[2][4] = {};
 #pragma unroll
-            for (int c = 0; c < HC / 32; ++c) {
-                float x[32];
-                tm_ld32(tO + lanes + HC * half + 32 * c, x);
+            for (int qq = 0; qq < 16; ++qq) {
+                const int q = 16 * hq + qq;
+                const float2 a = *reinterpret_cast<const float2*>(At + q * Lay::kAPitch + 32 + r2);
+                const float4 b = *reinterpret_cast<const float4*>(Tm + q * Lay::kTPitch + c4);
+                const float av[2] = {a.x, a.y}, bv[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
-                for (int j4 = 0; j4 < 8; ++j4) {
-                    float y[4];
+                for (int i2 = 0; i2 < 2; ++i2)
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int v = HC * half + 32 * c + 4 * j4 + e;
-                        y[e] = gated ? x[4 * j4 + e] * rinv * Gate[t * VC + (v ^ (t & 31))] : x[4 * j4 + e];
-                    }
-                    srow[8 * c + j4] = make_uint2(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]));
-                }
+                    for (int c = 0; c < 4; ++c) acc[i2][c] = fmaf(av[i2], bv[c], acc[i2][c]);
             }
+#pragma unroll
+            for (int i2 = 0; i2 < 2; ++i2)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) acc[i2][c] += __shfl_xor_sync(0xffffffffu, acc[i2][c], 1);
+            float m[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) m[c] = hq ? acc[1][c] : acc[0][c];
+            *reinterpret_cast<float4*>(Mb + (r2 + hq) * 32 + c4) = make_float4(m[0], m[1], m[2], m[3]);
+        }
+        __syncthreads();
+        {
+            const int hq = tid & 1, r2 = 2 * (tid >> 4), c4 = 4 * ((tid >> 1) & 7);
+            float acc[2][4] = {};
+#pragma unroll
+            for (int qq = 0; qq < 16; ++qq) {
+                const int q = 16 * hq + qq;
+                const float a0 = Tm[(32 + r2) * Lay::kTPitch + 32 + q];
+                const float a1 = Tm[(33 + r2) * Lay::kTPitch + 32 + q];
+                const float4 b = *reinterpret_cast<const float4*>(Mb + q * 32 + c4);
+                const float av[2] = {a0, a1}, bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+                for (int i2 = 0; i2 < 2; ++i2)
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) acc[i2][c] = fmaf(av[i2], bv[c], acc[i2][c]);
+            }
+#pragma unroll
+            for (int i2 = 0; i2 < 2; ++i2)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) acc[i2][c] += __shfl_xor_sync(0xffffffffu, acc[i2][c], 1);
+            float m[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) m[c] = hq ? acc[1][c] : acc[0][c];
+            *reinterpret_cast<float4*>(Tm + (32 + r2 + hq) * Lay::kTPitch + c4) =
+                make_float4(-m[0], -m[1], -m[2], -m[3]);
+        }
+        __syncthreads();
+        // (d) T hi | lo tiles [64 t][64 s]
+#pragma unroll
+        for (int e = tid; e < kC * 8; e += kThreads) {
+            const int t = e >> 3, j = e & 7;
+            const float4 a = *reinterpret_cast<const float4*>(Tm + t * Lay::kTPitch + 8 * j);
+            const float4 b = *reinterpret_cast<const float4*>(Tm + t * Lay::kTPitch + 8 * j + 4);
+            const float x[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+            uint4 hi, lo;
+            split8(x, hi, lo);
+            *reinterpret_cast<uint4*>(sm + Lay::kTHi + swz_chunk(t, j, kC)) = hi;
+            *reinterpret_cast<uint4*>(sm + Lay::kTLo + swz_chunk(t, j, kC)) = lo;
+        }
+        sync_for_mma();
+
+        // ---- MMA 2: V'^T = B^T T^T ----
+        if (tid == 0) {
+            gemm_split(tVp, sbase + Lay::kBHi, sbase + Lay::kBLo, VC, sbase + Lay::kTHi, sbase + Lay::kTLo, kC, 64,
+                       kC, false);
+            commit(bar);
+        }
+        if (wait_products()) break;
+
+        // ---- phase 4: V'^T hi | lo (in place of B^T) ----
+        if (col_lane) {
+            float x[32];
+            tm_ld32(tVp + lanes + 32 * hh, x);
+            put_row64(Lay::kBHi, Lay::kBLo, row, VC, 32 * hh, x);
+        }
+        sync_for_mma();
+
+        // ---- MMA 3: S^T += V'^T K~, O^T += V'^T R~^T; meanwhile the next chunk's loads ----
+        if (tid == 0) {
+            const uint32_t vH = sbase + Lay::kBHi, vL = sbase + Lay::kBLo;
+            gemm_split(tS, vH, vL, VC, sbase + Lay::kKtHi, sbase + Lay::kKtLo, 128, 128, kC, true);
+            gemm_split(tO, vH, vL, VC, sbase + Lay::kRt, sbase + Lay::kRt + kC * 128, kC, 64, kC, true);
+            commit(bar);
+        }
+        if (more) load_chunk(c0 + kC);
+        if (wait_products()) break;
+
+        // ---- phase 5: O^T into the output rows (FP32 [t][v]); the state images
+        //      for the next chunk ----
+        if (col_lane) {
+            float x[32];
+            tm_ld32(tO + lanes + 32 * hh, x);
+#pragma unroll
+            for (int u = 0; u < 32; ++u) Stage[(32 * hh + u) * Lay::kStagePitch + row] = x[u];
             if (more) {
 #pragma unroll
                 for (int c = 0; c < 2; ++c) {
-                    const int kd0 = 64 * half + 32 * c;
-                    float x[32];
+                    const int kd0 = 64 * hh + 32 * c;
                     tm_ld32(tS + lanes + kd0, x);
                     put_images(row, kd0, x);
                 }
             }
         }
         __syncthreads();
-        // the chunk's output rows, this CTA's columns
+        {
+            // the gated RMSNorm of rows t = warp + 8 j; lane holds VC / 32
+            // consecutive columns of a row
+            constexpr int PL = VC / 32;
+            float o[8][PL];
+            float ss[8];
 #pragma unroll
-        for (int e = tid; e < kC * (VC / 4); e += kThreads) {
-            const int t = e / (VC / 4), q4 = e % (VC / 4);
-            if (t < n)
-                *reinterpret_cast<uint2*>(p.out + ms.row[t] * p.out_stride + h * kV + cb + 4 * q4) =
-                    Stage[t * Lay::kStagePitch + q4];
+            for (int j = 0; j < 8; ++j) {
+                const float* src = Stage + (warp + 8 * j) * Lay::kStagePitch + PL * lane;
+                if constexpr (PL == 4) {
+                    const float4 f = *reinterpret_cast<const float4*>(src);
+                    o[j][0] = f.x; o[j][1] = f.y; o[j][2] = f.z; o[j][3] = f.w;
+                } else {
+                    const float2 f = *reinterpret_cast<const float2*>(src);
+                    o[j][0] = f.x; o[j][1] = f.y;
+                }
+                ss[j] = 0.f;
+#pragma unroll
+                for (int e = 0; e < PL; ++e) ss[j] = fmaf(o[j][e], o[j][e], ss[j]);
+            }
+            if (gated) {
+#pragma unroll
+                for (int m = 16; m >= 1; m >>= 1)
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) ss[j] += __shfl_xor_sync(0xffffffffu, ss[j], m);
+            }
+            if constexpr (CL > 1) {
+                // the other CTA's half of each row's sum of squares (distributed
+                // shared memory; the buffer alternates with the chunk parity, so the
+                // peer's next write to it comes after the next chunk's barrier)
+                if (gated && lane < 8) {
+                    float mine = ss[0];
+#pragma unroll
+                    for (int j = 1; j < 8; ++j) mine = lane == j ? ss[j] : mine;
+                    ms.ssq_cta[cpar][warp + 8 * lane] = mine;
+                }
+                cg::cluster_group cl = cg::this_cluster();
+                cl.sync();
+                if (gated) {
+                    const float* peer = cl.map_shared_rank(&ms.ssq_cta[cpar][0], rank ^ 1);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) ss[j] += peer[warp + 8 * j];
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int t = warp + 8 * j;
+                if (t >= n) continue;
+                float y[PL];
+                if (gated) {
+                    const float rinv = rsqrtf(ss[j] * (1.0f / kV) + p.eps);
+                    float zz[4];
+                    unpack4(Zq[t * Lay::kZStride + (PL * lane) / 4], zz);
+#pragma unroll
+                    for (int e = 0; e < PL; ++e) {
+                        const int v = PL * lane + e;
+                        const float zv = PL == 4 ? zz[e] : ((lane & 1) ? zz[2 + e] : zz[e]);
+                        y[e] = o[j][e] * rinv * ms.wn[v] * silu(zv);
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < PL; ++e) y[e] = o[j][e];
+                }
+                __nv_bfloat16* dst = p.out + ms.row[t] * p.out_stride + h * kV + cb + PL * lane;
+                if constexpr (PL == 4) {
+                    *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]));
+                } else {
+                    *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(y[0], y[1]);
+                }
+            }
         }
         fence_before();
         __syncthreads();
@@ -859,12 +960,12 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_chunked_kernel(const 
     }
 
     // ---- the final state to its slot (rounded once), then release TMEM ----
-    if (ok && wsl >= 0 && state_warp) {
+    if (ok && wsl >= 0 && col_lane) {
         StateT* dst =
             static_cast<StateT*>(p.pool) + (wsl * p.H_v + h) * static_cast<int64_t>(kK * kV) + cb + row;
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
-            const int kd0 = 64 * half + 32 * c;
+            const int kd0 = 64 * hh + 32 * c;
             float x[32];
             tm_ld32(tS + lanes + kd0, x);
 #pragma unroll
