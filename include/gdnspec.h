@@ -273,9 +273,9 @@ GDNSPEC_API gdn_status gdn_prefill(
  * Arguments, layouts, the caller contract and the status bits are those of
  * gdn_prefill; in addition GDN_FLAG_TIMEOUT reports a tensor-core wait that
  * ran past its bound.  One CTA per (sequence, v-head) unit, holding the
- * whole 512-column tensor memory of its SM (~214 KiB of shared memory); with
+ * whole 512-column tensor memory of its SM (~218 KiB of shared memory); with
  * fewer units than half the device's SMs, two CTAs per unit as a cluster,
- * each with 64 of the value columns (~164 KiB of shared memory each).  The
+ * each with 64 of the value columns (~210 KiB of shared memory each).  The
  * results do not depend on which form runs beyond FP32 rounding order.
  * Asynchronous on `stream`, allocates nothing.
  */
