@@ -867,7 +867,7 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="bs32_t8_bf16")
     ap.add_argument("--split", type=lambda x: int(x, 0), default=0,
-                    help="decode workloads: dims.split (0 = the library's choice; 1, 2, 4, 8, 0x102, 0x104)")
+                    help="decode workloads: dims.split (0 = the library's choice; 1, 2, 4, 8, 0x102, 0x104, 0x201, 0x202)")
     ap.add_argument("--flags", type=lambda x: int(x, 0), default=GDN_PRE_INDEX | GDN_PRE_TOKENS | GDN_PRE_STATE,
                     help="decode and conv workloads: dims.flags (default 7 = GDN_PRE_INDEX | GDN_PRE_TOKENS | "
                          "GDN_PRE_STATE: the resident inputs and the rotating sets' disjoint state and conv slots are "

@@ -24,6 +24,7 @@ GDN_FLAG_TOKEN_ROW = 8
 GDN_FLAG_TIMEOUT = 16
 GDN_FLAG_DRAIN = 32
 GDN_SPLIT_NARROW = 0x100     # dims.split flag: 8 V columns per warp (small batches)
+GDN_SPLIT_HALFK = 0x200      # dims.split flag (with 2): half of the K rows per warp (small batches)
 GDN_PRE_INDEX = 0x1          # dims.flags: the index tables were not written by the preceding kernel
 GDN_PRE_TOKENS = 0x2         # dims.flags (with GDN_PRE_INDEX): nor were the token inputs
 GDN_PRE_STATE = 0x4          # dims.flags (with GDN_PRE_INDEX): nor were the state slots this call reads

@@ -83,20 +83,29 @@ constexpr int64_t kTile = static_cast<int64_t>(kK) * kV;
 // .. R-1 (G row groups, R = 128 / G rows per lane).  The lane bits above the
 // column group are the row group in both layouts, so the reduce-scatter over
 // lane bits 4, 3, 2 means the same in both.
-template <int NCW>
+//
+// With KS = 2 (the half-K layout, 16 columns per warp) a warp owns half of
+// the K rows of its columns: warps w and w + W/2 of a CTA hold rows 0-63 and
+// 64-127, lane rows kq 64 + rg + 8 j (kq the half), 8 rows per lane, and
+// the two warps add their partial dot products through shared memory.
+template <int NCW, int KS = 1>
 struct Lanes {
     static_assert(NCW == 16 || NCW == 8, "16 or 8 columns per warp");
+    static_assert(KS == 1 || (KS == 2 && NCW == 16), "the half-K layout has 16 columns per warp");
     static constexpr int kColGroups = NCW / 4;            // 4 or 2
     static constexpr int kRowGroups = 32 / kColGroups;    // 8 or 16
-    static constexpr int kRows = kK / kRowGroups;         // 16 or 8
+    static constexpr int kSpan = kK / KS;                 // K rows of one warp
+    static constexpr int kRows = kSpan / kRowGroups;      // 16, 8 (narrow) or 8 (half-K)
     // k^ / q^ sit in shared memory permuted so that a lane's rows are
     // contiguous (row -> R (row % G) + row / G), with 4 floats of padding after
     // every 16 (NCW = 16) or 32 (NCW = 8) positions: the row groups' 16-byte
     // chunks then spread evenly over the banks (one wavefront for 8 groups,
     // two for 16).
-    static constexpr int kPadEvery = NCW == 16 ? 16 : 32;
+    static constexpr int kPadEvery = (NCW == 16 && KS == 1) ? 16 : 32;
     __host__ __device__ static constexpr int pos(int p) { return p + (p / kPadEvery) * 4; }
-    __host__ __device__ static constexpr int perm(int row) { return pos((row % kRowGroups) * kRows + row / kRowGroups); }
+    __host__ __device__ static constexpr int perm(int row) {
+        return pos((row / kSpan) * kSpan + (row % kRowGroups) * kRows + (row % kSpan) / kRowGroups);
+    }
 };
 constexpr int kKPad = kK + kK / 4;           // room for either padding
 
@@ -113,15 +122,16 @@ struct alignas(16) Smem {
     float decay[kMaxT], beta[kMaxT], kq[kMaxT], red[kMaxT];
     int row[kMaxT];
     long long ws[kMaxT];
+    float xch[2][8][2][32];      // half-K layout: the warp pairs' partial dots, by token parity
 };
 
-template <typename StateT, int SPLIT, int NCW = kColsPerWarp>
+template <typename StateT, int SPLIT, int NCW = kColsPerWarp, int KS = 1>
 struct Config {
-    static constexpr int kWarps = kV / NCW / SPLIT;
+    static constexpr int kWarps = kV / NCW / SPLIT * KS;
     static constexpr int kThreads = 32 * kWarps;
-    // each warp stages its 128 x 16 block of a token's state for the tensor store
+    // each warp stages its (128 / KS) x NCW block of a token's state for the tensor store
     static constexpr size_t kStageOffset = (sizeof(Smem) + 127) / 128 * 128;
-    static constexpr size_t kStageElems = static_cast<size_t>(kK) * NCW;
+    static constexpr size_t kStageElems = static_cast<size_t>(kK / KS) * NCW;
     // + 128 bytes so that the staging buffers can start on a 128-byte boundary
     static constexpr size_t kSmem = kStageOffset + kWarps * kStageElems * sizeof(StateT) + 128;
 };
@@ -255,7 +265,7 @@ __device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
 // Per-token prologue arithmetic for token t of unit (i, h), one warp: the raw
 // quads are this lane's 4 elements of q, k (key head), v and z (v-head);
 // `ws` is the slot that receives the state after this token (-1: none).
-template <int NCW = kColsPerWarp>
+template <int NCW = kColsPerWarp, int KS = 1>
 __device__ __forceinline__ void prologue_token_f(Smem& s, const Params& p, int h, int t, int r, int lane,
                                                  float (&qv)[4], float (&kv)[4], const float (&vv)[4], uint2 zraw,
                                                  long long ws) {
@@ -284,8 +294,8 @@ __device__ __forceinline__ void prologue_token_f(Smem& s, const Params& p, int h
     for (int e = 0; e < 4; ++e) { qv[e] *= rq; kv[e] *= rk; }
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-        s.q[t][Lanes<NCW>::perm(lane * 4 + e)] = qv[e];
-        s.k[t][Lanes<NCW>::perm(lane * 4 + e)] = kv[e];
+        s.q[t][Lanes<NCW, KS>::perm(lane * 4 + e)] = qv[e];
+        s.k[t][Lanes<NCW, KS>::perm(lane * 4 + e)] = kv[e];
     }
     *reinterpret_cast<float4*>(&s.v[t][lane * 4]) = make_float4(vv[0], vv[1], vv[2], vv[3]);
     s.z[t][lane] = zraw;
@@ -300,14 +310,14 @@ __device__ __forceinline__ void prologue_token_f(Smem& s, const Params& p, int h
     }
 }
 
-template <int NCW = kColsPerWarp>
+template <int NCW = kColsPerWarp, int KS = 1>
 __device__ __forceinline__ void prologue_token(Smem& s, const Params& p, int h, int t, int r, int lane,
                                                uint2 qraw, uint2 kraw, uint2 vraw, uint2 zraw, long long ws) {
     float qv[4], kv[4], vv[4];
     unpack_bf16x4(qraw, qv);
     unpack_bf16x4(kraw, kv);
     unpack_bf16x4(vraw, vv);
-    prologue_token_f<NCW>(s, p, h, t, r, lane, qv, kv, vv, zraw, ws);
+    prologue_token_f<NCW, KS>(s, p, h, t, r, lane, qv, kv, vv, zraw, ws);
 }
 
 // The state in this lane's block to slot ws (skip -1).  With a staging
@@ -316,10 +326,10 @@ __device__ __forceinline__ void prologue_token(Smem& s, const Params& p, int h, 
 // lane hands it to the tensor-memory-access unit, which writes the strided
 // block to the slot; the buffer is reused once that store has read it.
 // Without one, every lane stores its rows itself.
-template <typename StateT, int NCW>
-__device__ __forceinline__ void write_slot(const float (&S)[Lanes<NCW>::kRows][4], const Params& p, long long ws,
-                                           int h, int lane, int col0, int rank, StateT* stage) {
-    using L = Lanes<NCW>;
+template <typename StateT, int NCW, int KS = 1>
+__device__ __forceinline__ void write_slot(const float (&S)[Lanes<NCW, KS>::kRows][4], const Params& p, long long ws,
+                                           int h, int lane, int col0, int rank, StateT* stage, int kq = 0) {
+    using L = Lanes<NCW, KS>;
     const int cgi = lane % L::kColGroups;
     const int rg = lane / L::kColGroups;
     if (ws >= p.num_slots) raise_flag(p, rank, GDN_FLAG_SLOT_RANGE);
@@ -333,12 +343,13 @@ __device__ __forceinline__ void write_slot(const float (&S)[Lanes<NCW>::kRows][4
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             __syncwarp();
             if (lane == 0)
-                tma_store_box(&p.pool_map, stage, col0 - 4 * cgi, static_cast<int>((ws * p.H_v + h) * kK));
+                tma_store_box(&p.pool_map, stage, col0 - 4 * cgi,
+                              static_cast<int>((ws * p.H_v + h) * kK + kq * L::kSpan));
         } else {
             StateT* d = static_cast<StateT*>(p.pool) + (ws * p.H_v + h) * kTile + col0;
 #pragma unroll
             for (int r = 0; r < L::kRows; ++r)
-                StateIO<StateT>::store4(d + static_cast<int64_t>(rg + L::kRowGroups * r) * kV, S[r]);
+                StateIO<StateT>::store4(d + static_cast<int64_t>(kq * L::kSpan + rg + L::kRowGroups * r) * kV, S[r]);
         }
     }
 }
@@ -349,10 +360,11 @@ __device__ __forceinline__ void write_slot(const float (&S)[Lanes<NCW>::kRows][4
 // write while token t's partial products are formed (both only read S), and
 // the state after token t is left for the next call (or write_slot after the
 // last token): one CTA per SM waits on nothing between the two.
-template <typename StateT, int NCW = kColsPerWarp, bool PIPE = false>
-__device__ __forceinline__ void token_step(float (&S)[Lanes<NCW>::kRows][4], Smem& s, const Params& p, int t,
-                                           int h, int lane, int col0, int row0, int rank, StateT* stage) {
-    using L = Lanes<NCW>;
+template <typename StateT, int NCW = kColsPerWarp, bool PIPE = false, int KS = 1>
+__device__ __forceinline__ void token_step(float (&S)[Lanes<NCW, KS>::kRows][4], Smem& s, const Params& p, int t,
+                                           int h, int lane, int col0, int row0, int rank, StateT* stage,
+                                           int kq = 0, int pair = 0) {
+    using L = Lanes<NCW, KS>;
     const int cgi = lane % L::kColGroups;
     const int rg = lane / L::kColGroups;
     long long pws = -1;                  // PIPE: the previous token's slot, staged below
@@ -371,7 +383,7 @@ __device__ __forceinline__ void token_step(float (&S)[Lanes<NCW>::kRows][4], Sme
     const int d_own = (lane >> 4) & 1; // ... and which dot product (0: k, 1: q)
     const float decay = s.decay[t];
     const float beta = s.beta[t];
-    const float kq = s.kq[t];
+    const float kq_dot = s.kq[t];
 
     // partial S^T k^ and S^T q^ over this lane's 16 rows, 4 columns each
     float x[8];
@@ -408,7 +420,8 @@ __device__ __forceinline__ void token_step(float (&S)[Lanes<NCW>::kRows][4], Sme
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             __syncwarp();
             if (lane == 0)
-                tma_store_box(&p.pool_map, stage, col0 - 4 * cgi, static_cast<int>((pws * p.H_v + h) * kK));
+                tma_store_box(&p.pool_map, stage, col0 - 4 * cgi,
+                              static_cast<int>((pws * p.H_v + h) * kK + kq * L::kSpan));
         }
     }
     // reduce-scatter over the row groups on lane bits 4, 3, 2: afterwards the
@@ -444,10 +457,20 @@ __device__ __forceinline__ void token_step(float (&S)[Lanes<NCW>::kRows][4], Sme
         dot = keep + __shfl_xor_sync(kFull, send, 4);
     }
     if constexpr (NCW == 8) dot += __shfl_xor_sync(kFull, dot, 2);
+    if constexpr (KS == 2) {
+        // the other half of K: the partner warp's partial sums, through shared
+        // memory (by token parity, so that a warp's next write never meets a
+        // read of the partner's that is still pending), one named barrier per
+        // warp pair
+        float* xch = &s.xch[t & 1][pair][0][0];
+        xch[kq * 32 + lane] = dot;
+        asm volatile("bar.sync %0, 64;" ::"r"(1 + pair) : "memory");
+        dot += xch[(kq ^ 1) * 32 + lane];
+    }
     // delta rule on the k lanes; readout on the q lanes
     const float vp = beta * (s.v[t][col0 + c_own] - decay * dot);   // valid where d_own == 0
     const float vp_pair = __shfl_xor_sync(kFull, vp, 16);
-    if (d_own == 1) s.o[t][col0 + c_own] = fmaf(decay, dot, kq * vp_pair);
+    if (d_own == 1 && kq == 0) s.o[t][col0 + c_own] = fmaf(decay, dot, kq_dot * vp_pair);
     float vpc[4];
 #pragma unroll
     for (int c = 0; c < 4; ++c) vpc[c] = __shfl_sync(kFull, vp, cgi + 4 * c);
@@ -469,7 +492,7 @@ __device__ __forceinline__ void token_step(float (&S)[Lanes<NCW>::kRows][4], Sme
 
     // the state after token t goes to slot s.ws[t] (skip -1); with PIPE, during
     // the next token
-    if constexpr (!PIPE) write_slot<StateT, NCW>(S, p, s.ws[t], h, lane, col0, rank, stage);
+    if constexpr (!PIPE) write_slot<StateT, NCW, KS>(S, p, s.ws[t], h, lane, col0, rank, stage, kq);
 }
 
 // Gated RMSNorm epilogue over tokens 0 .. n-1 in shared memory: out = o *
@@ -632,12 +655,13 @@ __device__ __forceinline__ void conv_token(const Params& p, int bos, int t, cons
 //
 // Grid: one CTA per (unit, column slice); SPLIT CTAs of a unit form one cluster.
 // Block: 128 / NCW / SPLIT warps, each owning NCW of the unit's 128 V columns.
-template <typename StateT, int SPLIT, bool CONV = false, int NCW = kColsPerWarp, bool PIPE = false>
-__global__ void __launch_bounds__(Config<StateT, SPLIT, NCW>::kThreads, NCW == kColsPerWarp ? 2 * SPLIT : SPLIT)
+template <typename StateT, int SPLIT, bool CONV = false, int NCW = kColsPerWarp, bool PIPE = false, int KS = 1>
+__global__ void __launch_bounds__(Config<StateT, SPLIT, NCW, KS>::kThreads, 512 / Config<StateT, SPLIT, NCW, KS>::kThreads)
 gdn_spec_decode_kernel(const __grid_constant__ Params p) {
-    using C = Config<StateT, SPLIT, NCW>;
-    using L = Lanes<NCW>;
+    using C = Config<StateT, SPLIT, NCW, KS>;
+    using L = Lanes<NCW, KS>;
     constexpr int W = C::kWarps;
+    constexpr int WC = W / KS;                                  // warps per K half: column blocks of the CTA
     extern __shared__ __align__(128) unsigned char smem_raw[];
     Smem& s = *reinterpret_cast<Smem*>(smem_raw);
 
@@ -648,10 +672,12 @@ gdn_spec_decode_kernel(const __grid_constant__ Params p) {
     const int i = unit / p.H_v;
     const int h = unit - i * p.H_v;
     const int cgi = lane % L::kColGroups;  // column group: 4 consecutive columns
-    const int rg = lane / L::kColGroups;   // row group: K rows rg + G j
-    const int wg = rank * W + warp;        // this warp's NCW-column block
+    const int rg = lane / L::kColGroups;   // row group: K rows kq 64 + rg + G j
+    const int kq = warp / WC;              // this warp's half of K (0 unless KS = 2)
+    const int wg = rank * WC + warp % WC;  // this warp's NCW-column block
     const int col0 = wg * NCW + cgi * 4;
-    const int row0 = rg * L::kRows;        // where those rows sit in the permuted k^ / q^
+    const int krow0 = kq * L::kSpan + rg;  // this lane's first K row
+    const int row0 = kq * L::kSpan + rg * L::kRows;   // where its rows sit in the permuted k^ / q^
 
     // Launched with programmatic stream serialization: this CTA may become
     // resident while the previous kernel in the stream is still running.  It
@@ -731,7 +757,7 @@ gdn_spec_decode_kernel(const __grid_constant__ Params p) {
     if (pre_state || !pre_tokens) {
 #pragma unroll
         for (int r = 0; r < L::kRows; ++r)
-            StateIO<StateT>::load4(src + static_cast<int64_t>(rg + L::kRowGroups * r) * kV + col0, S[r]);
+            StateIO<StateT>::load4(src + static_cast<int64_t>(krow0 + L::kRowGroups * r) * kV + col0, S[r]);
     }
     if (pre_state && !pre_tokens) dep_wait();
 
@@ -761,11 +787,11 @@ gdn_spec_decode_kernel(const __grid_constant__ Params p) {
                     const uint2 zraw = p.z != nullptr
                                            ? ldg_quad(p.z + r * p.z_stride + static_cast<int64_t>(h) * kV + lane * 4)
                                            : make_uint2(0, 0);
-                    prologue_token_f<NCW>(s, p, h, t, r, lane, y[0], y[1], y[2], zraw, ws);
+                    prologue_token_f<NCW, KS>(s, p, h, t, r, lane, y[0], y[1], y[2], zraw, ws);
                 } else {
                     uint2 qraw, kraw, vraw, zraw;
                     load_token_quads(p, r, kh, h, lane, qraw, kraw, vraw, zraw);
-                    prologue_token<NCW>(s, p, h, t, r, lane, qraw, kraw, vraw, zraw, ws);
+                    prologue_token<NCW, KS>(s, p, h, t, r, lane, qraw, kraw, vraw, zraw, ws);
                 }
             }
         }
@@ -775,7 +801,7 @@ gdn_spec_decode_kernel(const __grid_constant__ Params p) {
         if (!pre_state) {
 #pragma unroll
             for (int r = 0; r < L::kRows; ++r)
-                StateIO<StateT>::load4(src + static_cast<int64_t>(rg + L::kRowGroups * r) * kV + col0, S[r]);
+                StateIO<StateT>::load4(src + static_cast<int64_t>(krow0 + L::kRowGroups * r) * kV + col0, S[r]);
         }
     }
     // publishes the prologue; every CTA of the cluster checks every token row,
@@ -815,8 +841,9 @@ gdn_spec_decode_kernel(const __grid_constant__ Params p) {
     StateT* stage = reinterpret_cast<StateT*>(smem_raw + C::kStageOffset +
                                               ((128u - (smem_addr(smem_raw) & 127u)) & 127u)) +
                     warp * C::kStageElems;
-    for (int t = 0; t < q_len; ++t) token_step<StateT, NCW, PIPE>(S, s, p, t, h, lane, col0, row0, rank, stage);
-    if constexpr (PIPE) write_slot<StateT, NCW>(S, p, s.ws[q_len - 1], h, lane, col0, rank, stage);
+    for (int t = 0; t < q_len; ++t)
+        token_step<StateT, NCW, PIPE, KS>(S, s, p, t, h, lane, col0, row0, rank, stage, kq, warp % WC);
+    if constexpr (PIPE) write_slot<StateT, NCW, KS>(S, p, s.ws[q_len - 1], h, lane, col0, rank, stage, kq);
 
     // ---- gated RMSNorm epilogue ----
     __syncthreads();                                           // s.o of this CTA complete
@@ -889,10 +916,10 @@ __global__ void __launch_bounds__(256, 2) gdn_prefill_kernel(const Params p) {
 
 // ---- host side ----------------------------------------------------------------
 
-template <typename StateT, int SPLIT, bool CONV = false, int NCW = kColsPerWarp, bool PIPE = false>
+template <typename StateT, int SPLIT, bool CONV = false, int NCW = kColsPerWarp, bool PIPE = false, int KS = 1>
 cudaError_t launch(const Params& p, int64_t units, cudaStream_t stream) {
-    using C = Config<StateT, SPLIT, NCW>;
-    auto kernel = gdn_spec_decode_kernel<StateT, SPLIT, CONV, NCW, PIPE>;
+    using C = Config<StateT, SPLIT, NCW, KS>;
+    auto kernel = gdn_spec_decode_kernel<StateT, SPLIT, CONV, NCW, PIPE, KS>;
     if (C::kSmem > 48 * 1024) {
         // opt in to more than 48 KB of dynamic shared memory, once per device
         static bool done[64] = {false};
@@ -951,6 +978,12 @@ cudaError_t launch_split(const Params& p, int64_t units, int split, cudaStream_t
     case 4: return launch<StateT, 4>(p, units, stream);
     case GDN_SPLIT_NARROW | 2: return launch<StateT, 2, false, 8>(p, units, stream);
     case GDN_SPLIT_NARROW | 4: return launch<StateT, 4, false, 8>(p, units, stream);
+    case GDN_SPLIT_HALFK | 1:
+        return pipelined(units) ? launch<StateT, 1, false, kColsPerWarp, true, 2>(p, units, stream)
+                                : launch<StateT, 1, false, kColsPerWarp, false, 2>(p, units, stream);
+    case GDN_SPLIT_HALFK | 2:
+        return pipelined(2 * units) ? launch<StateT, 2, false, kColsPerWarp, true, 2>(p, units, stream)
+                                    : launch<StateT, 2, false, kColsPerWarp, false, 2>(p, units, stream);
     default: return launch<StateT, 8>(p, units, stream);
     }
 }
@@ -974,7 +1007,8 @@ bool aligned(const void* ptr, uintptr_t a) { return (reinterpret_cast<uintptr_t>
 // cuTensorMapEncodeTiled is reached through the runtime's driver entry point
 // (no link against the driver library); maps are cached per host thread for
 // the last few pools, so a steady stream of calls encodes nothing.
-gdn_status make_pool_map(Params& p, void* pool, int64_t num_slots, int32_t H_v, gdn_dtype dt, int cols) {
+gdn_status make_pool_map(Params& p, void* pool, int64_t num_slots, int32_t H_v, gdn_dtype dt, int cols,
+                         int box_rows = kK) {
     using Encode = PFN_cuTensorMapEncodeTiled_v12000;
     static const Encode encode = [] {
         void* fn = nullptr;
@@ -991,20 +1025,20 @@ gdn_status make_pool_map(Params& p, void* pool, int64_t num_slots, int32_t H_v, 
     struct Entry {
         const void* pool;
         int64_t rows;
-        int dt, cols;
+        int dt, cols, box_rows;
         CUtensorMap map;
     };
     thread_local Entry cache[4] = {};
     thread_local int next = 0;
     for (const Entry& e : cache)
-        if (e.pool == pool && e.rows == rows && e.dt == dt && e.cols == cols) {
+        if (e.pool == pool && e.rows == rows && e.dt == dt && e.cols == cols && e.box_rows == box_rows) {
             p.pool_map = e.map;
             return GDN_OK;
         }
     const size_t elem = dt == GDN_F32 ? 4 : 2;
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kV), static_cast<cuuint64_t>(rows)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kV * elem)};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(cols), static_cast<cuuint32_t>(kK)};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(cols), static_cast<cuuint32_t>(box_rows)};
     const cuuint32_t estr[2] = {1, 1};
     const CUtensorMapDataType type = dt == GDN_F32    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
                                      : dt == GDN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
@@ -1014,21 +1048,25 @@ gdn_status make_pool_map(Params& p, void* pool, int64_t num_slots, int32_t H_v, 
                CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return GDN_ERR_CUDA;
-    cache[next] = Entry{pool, rows, static_cast<int>(dt), cols, map};
+    cache[next] = Entry{pool, rows, static_cast<int>(dt), cols, box_rows, map};
     next = (next + 1) % 4;
     p.pool_map = map;
     return GDN_OK;
 }
 
 // One CTA per unit, each warp owning 16 V columns, at every batch size
-// measured (4 to 256 sequences of 16 v-heads) but one: an FP32 state with at
-// most 64 units (4 sequences of 16 v-heads) runs the narrow layout over 2-CTA
-// clusters (BS=4: 13.9 -> 11.6 us).  Splitting the 16-column warps over a
-// cluster shortens no per-token chain and adds cluster barriers; narrow warps
-// with 16-bit states store 16-byte rows, whose tensor stores cost more than
-// the shorter chain saves.
+// measured (4 to 256 sequences of 16 v-heads) but two: an FP32 state with at
+// most 64 units (4 sequences of 16 v-heads) runs the half-K layout over 2-CTA
+// clusters (BS=4: 9.40 us with the narrow layout, 9.08 us), and with at most
+// 128 units the half-K layout in one 16-warp CTA (BS=8: 13.52 -> 13.06 us).
+// Splitting the 16-column warps over a cluster shortens no per-token chain and
+// adds cluster barriers; with 16-bit states neither half-K form nor the narrow
+// layout beats one 8-warp CTA per unit (BS=4 bf16: 7.64 us; half-K 7.98 /
+// 8.31 us; narrow 9.47 us).
 int choose_split(int64_t units, gdn_dtype dt) {
-    return (dt == GDN_F32 && units <= 64) ? (GDN_SPLIT_NARROW | 2) : 1;
+    if (dt == GDN_F32 && units <= 64) return GDN_SPLIT_HALFK | 2;
+    if (dt == GDN_F32 && units <= 128) return GDN_SPLIT_HALFK | 1;
+    return 1;
 }
 
 gdn_status check_dims(const gdn_dims* d) {
@@ -1043,7 +1081,8 @@ gdn_status check_dims(const gdn_dims* d) {
         return GDN_ERR_BAD_SHAPE;
     if (d->K != kK || d->V != kV) return GDN_ERR_UNSUPPORTED;
     if (!(d->split == 0 || d->split == 1 || d->split == 2 || d->split == 4 || d->split == 8 ||
-          d->split == (GDN_SPLIT_NARROW | 2) || d->split == (GDN_SPLIT_NARROW | 4)))
+          d->split == (GDN_SPLIT_NARROW | 2) || d->split == (GDN_SPLIT_NARROW | 4) ||
+          d->split == (GDN_SPLIT_HALFK | 1) || d->split == (GDN_SPLIT_HALFK | 2)))
         return GDN_ERR_UNSUPPORTED;
     if (static_cast<int64_t>(d->batch) * d->H_v * 8 > 0x7fffffffLL) return GDN_ERR_BAD_SHAPE;
     return GDN_OK;
@@ -1169,7 +1208,8 @@ gdn_status gdn_spec_decode(const void* q, const void* k, const void* v, const vo
     const int64_t units = static_cast<int64_t>(dims->batch) * dims->H_v;
     const int split = dims->split ? dims->split : choose_split(units, state_dtype);
     const gdn_status ms = make_pool_map(p, state_pool, dims->num_slots, dims->H_v, state_dtype,
-                                        (split & GDN_SPLIT_NARROW) ? 8 : kColsPerWarp);
+                                        (split & GDN_SPLIT_NARROW) ? 8 : kColsPerWarp,
+                                        (split & GDN_SPLIT_HALFK) ? kK / 2 : kK);
     if (ms != GDN_OK) return ms;
     const cudaError_t err =
         by_state_dtype<DecodeLauncher>(state_dtype, p, units, split, reinterpret_cast<cudaStream_t>(stream));

@@ -49,8 +49,10 @@ extern "C" {
 #endif
 
 /* 2: gdn_spec_decode_split takes the state dtype; dims->split accepts GDN_SPLIT_NARROW
-   3: dims->flags (formerly reserved): GDN_PRE_INDEX, GDN_PRE_TOKENS, GDN_PRE_STATE */
-#define GDNSPEC_VERSION 3
+   3: dims->flags (formerly reserved): GDN_PRE_INDEX, GDN_PRE_TOKENS, GDN_PRE_STATE
+   4: dims->split accepts GDN_SPLIT_HALFK | 1 and | 2, the automatic choice for small
+      FP32 batches */
+#define GDNSPEC_VERSION 4
 
 #if defined(__GNUC__)
 #define GDNSPEC_API __attribute__((visibility("default")))
@@ -97,6 +99,16 @@ typedef enum { GDN_F32 = 0, GDN_BF16 = 1, GDN_F16 = 2 } gdn_dtype;
  * Same results up to FP32 rounding order.
  */
 #define GDN_SPLIT_NARROW 0x100
+
+/*
+ * dims->split flag (GDN_SPLIT_HALFK | 1 or | 2): each warp keeps 16 V columns
+ * but only half of their 128 K rows, the two warps of a column block adding
+ * their partial products through shared memory once per token, so its
+ * tensor stores keep the 16-column rows.  A unit's 16 warps run in one CTA
+ * (| 1) or over a 2-CTA cluster (| 2, half of a unit's work per SM).  Meant
+ * for small batches.  Same results up to FP32 rounding order.
+ */
+#define GDN_SPLIT_HALFK 0x200
 
 /*
  * dims->flags: what the caller promises about the kernel launched on the
@@ -153,9 +165,11 @@ typedef struct {
     int64_t q_stride, k_stride, v_stride, a_stride, b_stride, z_stride, out_stride;
     int32_t split;        /* CTAs per (sequence, v-head), one thread-block cluster:
                              0 = chosen from the batch size; else 1, 2, 4 or 8
-                             (each warp owns 16 V columns), or GDN_SPLIT_NARROW
+                             (each warp owns 16 V columns), GDN_SPLIT_NARROW
                              | 2 or | 4 (each warp owns 8 V columns: 16 warps
-                             per unit over 2 or 4 CTAs) */
+                             per unit over 2 or 4 CTAs), or GDN_SPLIT_HALFK | 1
+                             or | 2 (16 columns and half the K rows per warp:
+                             16 warps per unit in 1 or 2 CTAs) */
     int32_t flags;        /* 0, or GDN_PRE_INDEX [| GDN_PRE_TOKENS] [| GDN_PRE_STATE] (above); 0 for prefill */
 } gdn_dims;
 
@@ -355,8 +369,9 @@ GDNSPEC_API gdn_status gdn_spec_decode_conv(
 
 /*
  * The split code that gdn_spec_decode would use for these sizes and state
- * dtype (dims->split itself when it is not 0; else 1, or GDN_SPLIT_NARROW | 2
- * for an FP32 state with batch * H_v <= 64), or 0 for invalid dims or dtype.
+ * dtype (dims->split itself when it is not 0; else, for an FP32 state,
+ * GDN_SPLIT_HALFK | 2 with batch * H_v <= 64 and GDN_SPLIT_HALFK | 1 with
+ * batch * H_v <= 128; else 1), or 0 for invalid dims or dtype.
  * Host only; reads no device state.
  */
 GDNSPEC_API int32_t gdn_spec_decode_split(const gdn_dims* dims, gdn_dtype state_dtype);

@@ -97,6 +97,7 @@ def _call(lib, dims, *, ptr=0x1000, z=0x1000, w=0x1000, state_dtype=0):
     (dict(K=64), 3), (dict(V=256), 3), (dict(H_v=12, H_k=8), 2), (dict(max_T=9), 2),
     (dict(max_T=0), 2), (dict(spec_stride=0), 2), (dict(batch=-1), 2), (dict(num_slots=0), 2),
     (dict(split=3), 3), (dict(split=0x101), 3), (dict(split=0x108), 3), (dict(split=0x100), 3),
+    (dict(split=0x200), 3), (dict(split=0x204), 3), (dict(split=0x302), 3),
     (dict(flags=8), 2), (dict(flags=-1), 2), (dict(q_stride=-4), 2),
 ])
 def test_bad_dims_rejected(lib, over, code):
@@ -118,18 +119,22 @@ def test_empty_batch_is_a_no_op(lib):
 
 
 def test_explicit_split_is_reported(lib):
-    for s in (1, 2, 4, 8, binding.GDN_SPLIT_NARROW | 2, binding.GDN_SPLIT_NARROW | 4):
+    for s in (1, 2, 4, 8, binding.GDN_SPLIT_NARROW | 2, binding.GDN_SPLIT_NARROW | 4, binding.GDN_SPLIT_HALFK | 1,
+              binding.GDN_SPLIT_HALFK | 2):
         assert binding.chosen_split(_dims(split=s)) == s
     assert binding.chosen_split(_dims(K=64)) == 0
     assert binding.chosen_split(_dims(), 7) == 0
 
 
 def test_automatic_split():
-    """FP32 state with at most 64 units: the narrow layout over 2-CTA
-    clusters; everything else one CTA per unit."""
-    N2 = binding.GDN_SPLIT_NARROW | 2
-    assert binding.chosen_split(_dims(batch=4, H_v=16), binding.F32) == N2
-    assert binding.chosen_split(_dims(batch=5, H_v=16), binding.F32) == 1
+    """FP32 state: the half-K layout over 2-CTA clusters with at most 64
+    units, in one 16-warp CTA with at most 128; everything else one CTA of 8
+    warps per unit."""
+    H2, H1 = binding.GDN_SPLIT_HALFK | 2, binding.GDN_SPLIT_HALFK | 1
+    assert binding.chosen_split(_dims(batch=4, H_v=16), binding.F32) == H2
+    assert binding.chosen_split(_dims(batch=5, H_v=16), binding.F32) == H1
+    assert binding.chosen_split(_dims(batch=8, H_v=16), binding.F32) == H1
+    assert binding.chosen_split(_dims(batch=9, H_v=16), binding.F32) == 1
     assert binding.chosen_split(_dims(batch=4, H_v=16), binding.BF16) == 1
     assert binding.chosen_split(_dims(batch=4, H_v=16), binding.F16) == 1
 

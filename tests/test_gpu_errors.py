@@ -48,7 +48,7 @@ def _run_and_check(case, gpu_case, flag, skipped_seq=True, expect=None, split=0,
         assert bool((out.view(torch.int16)[rows] == OUT_SENTINEL).all())
 
 
-@pytest.mark.parametrize("split", [1, 8, 0x102])
+@pytest.mark.parametrize("split", [1, 8, 0x102, 0x202])
 def test_num_accepted_beyond_stride(split):
     case = _base()
     bad = dataclasses.replace(case, num_accepted=case.num_accepted.copy())
@@ -69,7 +69,7 @@ def test_bad_data_with_early_reads(flags):
     _run_and_check(case, bad, gdn.binding.GDN_FLAG_SLOT_RANGE, flags=flags)
 
 
-@pytest.mark.parametrize("split", [1, 8, 0x102])
+@pytest.mark.parametrize("split", [1, 8, 0x102, 0x202])
 def test_read_slot_out_of_range(split):
     case = _base()
     bad = dataclasses.replace(case, state_indices=case.state_indices.copy())
@@ -99,7 +99,7 @@ def test_q_len_beyond_max_T():
     _run_and_check(c2, gpu_case, gdn.binding.GDN_FLAG_QLEN)
 
 
-@pytest.mark.parametrize("split", [1, 4, 0x104])
+@pytest.mark.parametrize("split", [1, 4, 0x104, 0x201])
 def test_gathered_row_out_of_range(split):
     case = synth.make_case(batch=8, H_k=1, H_v=8, T=4, state_dtype=synth.F32, num_slots=64,
                            extra_rows=5, acc=[1, 2, 3, 4, 0, 1, 2, 3], seed=33)

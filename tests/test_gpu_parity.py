@@ -20,7 +20,7 @@ from tests.util import bf16_bits, bf16_values
 
 pytestmark = pytest.mark.gpu
 
-SPLITS = (1, 2, 4, 8, 0x102, 0x104)      # 0x100: GDN_SPLIT_NARROW (8 columns per warp)
+SPLITS = (1, 2, 4, 8, 0x102, 0x104, 0x201, 0x202)   # 0x100: GDN_SPLIT_NARROW (8 columns per warp); 0x200: GDN_SPLIT_HALFK
 
 
 def _invariants(case, pool_before, pool_after, out):
@@ -268,7 +268,7 @@ def test_deterministic(cuda_device):
     assert torch.equal(r[0][0], r[1][0]) and torch.equal(r[0][1], r[1][1])
 
 
-@pytest.mark.parametrize("split", [0, 0x102])
+@pytest.mark.parametrize("split", [0, 0x102, 0x202])
 def test_gate_and_input_extremes(cuda_device, split):
     """Each input at the end of its range, against the oracle: a + dt_bias above
     the softplus threshold (heads 0-3), per-token decays that underflow to 0
@@ -294,7 +294,7 @@ def test_gate_and_input_extremes(cuda_device, split):
     assert m["out_rel_l2"] < 5e-4
 
 
-@pytest.mark.parametrize("split", [1, 2, 0x102])
+@pytest.mark.parametrize("split", [1, 2, 0x102, 0x201, 0x202])
 @pytest.mark.parametrize("sd", [synth.F32, synth.BF16])
 def test_early_read_flags_change_no_bit(cuda_device, sd, split):
     """GDN_PRE_INDEX, with GDN_PRE_TOKENS and / or GDN_PRE_STATE, moves reads
