@@ -38,8 +38,11 @@
 //    mean-square over V is then combined through distributed shared memory.
 //    The narrow layout (NCW = 8) gives each warp 8 columns instead of 16: a
 //    unit's 16 warps run over a 2- or 4-CTA cluster with half the state per
-//    lane and one more butterfly step; it is the automatic choice for an FP32
-//    state with at most 64 units.
+//    lane and one more butterfly step.  The half-K layout (KS = 2) keeps 16
+//    columns per warp but gives each warp half of their K rows; the two warps
+//    of a column block add their partial products through shared memory once
+//    per token, and a unit's 16 warps run in one CTA or over a 2-CTA cluster.
+//    It is the automatic choice for an FP32 state with at most 128 units.
 //  * No device-side waits on flags, no traps: bad device data is skipped and
 //    reported through an optional status word.
 //  * Fused convolution (CONV = true, SPLIT = 1): each lane convolves its 12
