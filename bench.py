@@ -735,43 +735,66 @@ def run_gpu(args, rank, world, local_rank):
     # --- end to end through the public API with host buffers ---
     # every step: one pinned host-to-device copy of the step's inputs, the
     # call, and a device-to-host read of its output.  Copies run on their own
-    # streams, so step s+1's inputs travel while step s computes and step s's
-    # output travels back while step s+1 computes; events keep each set's
-    # buffers free until the step that last used them has finished.
+    # streams.  Steps go in groups of G = n_sets / 2 (two groups' sets in
+    # flight): a group's inputs travel while the previous group computes and
+    # its outputs travel back while the next one computes.  The compute stream
+    # waits on events only at group boundaries, so the calls of a group follow
+    # one another directly on the stream and each may start while the one
+    # before it drains; events keep each set's buffers free until the group
+    # that last used them has finished with them.
     up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     rt = CudaRuntime()
     hs, hu, hd = handle, up.cuda_stream, down.cuda_stream
-    h2d_done = [rt.event() for _ in range(n_sets)]
-    run_done = [rt.event() for _ in range(n_sets)]
-    d2h_done = [rt.event() for _ in range(n_sets)]
-    used = [False] * n_sets
+    G = max(n_sets // 2, 1)
+    n_groups = n_sets // G                              # groups whose sets are in flight at once
+    h2d_done = [rt.event() for _ in range(n_groups)]
+    run_done = [rt.event() for _ in range(n_groups)]
+    d2h_done = [rt.event() for _ in range(n_groups)]
+    used = [False] * n_groups
+    e2e_next = [0]                                      # the next step to issue
 
-    def e2e_step(s):
-        k = s % n_sets
-        st = sets[k]
-        if used[k]:
-            rt.wait(hu, run_done[k])                    # the set's inputs were consumed
-        rt.copy(st.packed.dev.data_ptr(), st.packed.host.data_ptr(), st.packed.total, rt.H2D, hu)
-        rt.record(h2d_done[k], hu)
-        rt.wait(hs, h2d_done[k])
-        if used[k]:
-            rt.wait(hs, d2h_done[k])                    # the set's previous output was read back
-        # the inputs were written by a copy that the stream waited for, not
+    def e2e_group(count):
+        s0 = e2e_next[0]
+        grp = (s0 // G) % n_groups                      # the slot whose sets this group uses
+        ks = [(s0 + j) % n_sets for j in range(count)]
+        if used[grp]:
+            rt.wait(hu, run_done[grp])                  # the sets' inputs were consumed
+        for k in ks:
+            st = sets[k]
+            rt.copy(st.packed.dev.data_ptr(), st.packed.host.data_ptr(), st.packed.total, rt.H2D, hu)
+        rt.record(h2d_done[grp], hu)
+        rt.wait(hs, h2d_done[grp])
+        if used[grp]:
+            rt.wait(hs, d2h_done[grp])                  # the sets' previous outputs were read back
+        # the inputs were written by copies that the stream waited for, not
         # by the preceding kernel, so the early reads stay valid
-        st.call(hs, flags)
-        rt.record(run_done[k], hs)
-        rt.wait(hd, run_done[k])
-        rt.copy(st.host_out.data_ptr(), st.out.data_ptr(), st.out.numel() * st.out.element_size(), rt.D2H, hd)
-        rt.record(d2h_done[k], hd)
-        used[k] = True
+        for k in ks:
+            sets[k].call(hs, flags)
+        rt.record(run_done[grp], hs)
+        rt.wait(hd, run_done[grp])
+        for k in ks:
+            st = sets[k]
+            rt.copy(st.host_out.data_ptr(), st.out.data_ptr(), st.out.numel() * st.out.element_size(), rt.D2H, hd)
+        rt.record(d2h_done[grp], hd)
+        used[grp] = True
+        e2e_next[0] += count
+
+    def e2e_run(steps_total):
+        # groups start at multiples of G so that a group's sets are always the
+        # same slot's; the first group may be shorter to get there
+        done = 0
+        while done < steps_total:
+            s0 = e2e_next[0]
+            count = min(G - s0 % G, steps_total - done)
+            e2e_group(count)
+            done += count
 
     def e2e_drain():
-        for k in range(n_sets):
-            if used[k]:
-                rt.wait(hs, d2h_done[k])
+        for g in range(n_groups):
+            if used[g]:
+                rt.wait(hs, d2h_done[g])
 
-    for s in range(3):
-        e2e_step(s)
+    e2e_run(max(3, G))
     e2e_drain()
     torch.cuda.synchronize()
     barrier()
@@ -779,8 +802,7 @@ def run_gpu(args, rank, world, local_rank):
     e0.record(stream)
     up.wait_event(e0)
     down.wait_event(e0)
-    for s in range(K):
-        e2e_step(s)
+    e2e_run(K)
     e2e_drain()
     e1.record(stream)
     torch.cuda.synchronize()
