@@ -124,6 +124,20 @@ def test_ragged_prompts_few_units(entry, sd):
     _check(entry, case, *_run(entry, case, reads, writes), writes)
 
 
+@pytest.mark.parametrize("H_k,ratio,lens", [
+    (3, 1, [37, 70, 5]),                                          # 9 units: 2-CTA clusters
+    (3, 4, [37, 70, 5]),                                          # 36 units
+    (4, 2, [37, 70, 5, 64, 1, 100, 9, 20, 33, 65, 2, 128]),      # 96 units: one CTA per unit
+], ids=["ratio1", "ratio4", "ratio2-96-units"])
+@pytest.mark.parametrize("entry", list(ENTRIES))
+def test_head_ratios(entry, H_k, ratio, lens):
+    """v-heads per key head other than 8 (H_v = ratio H_k, v-head h reads key
+    head h / ratio), FP32 state, in both launch forms of the chunked entry."""
+    case = _case(lens, synth.F32, H_k=H_k, H_v=H_k * ratio, seed=63 + ratio)
+    reads, writes = _slots(case, 10 + ratio)
+    _check(entry, case, *_run(entry, case, reads, writes), writes)
+
+
 @pytest.mark.parametrize("sd", [synth.F32, synth.BF16])
 @pytest.mark.parametrize("entry", list(ENTRIES))
 def test_long_prompts_weak_decay(entry, sd):
