@@ -121,6 +121,32 @@ def test_ragged_padding_pipelined_writes(cuda_device, sd):
     _full_check(case, cuda_device, 1)
 
 
+@pytest.mark.parametrize("sd", [synth.BF16, synth.F16, synth.F32])
+def test_single_token_steps(cuda_device, sd):
+    """max_T = 1 (ordinary decode as a one-token step), every state dtype: 30 %
+    padded slots, 640 units (more than one round of CTAs)."""
+    case = synth.make_case(batch=40, H_k=2, H_v=16, T=1, state_dtype=sd, num_slots=256, pad_prob=0.3, seed=35)
+    assert case.max_T == 1
+    _full_check(case, cuda_device, 0)
+
+
+@pytest.mark.parametrize("sd", [synth.BF16, synth.F16])
+def test_single_token_flags_change_no_bit(cuda_device, sd):
+    """One-token steps with ragged q_len in {0, 1}: the early-read flags change
+    no bit of out or of the pool."""
+    case = synth.make_case(batch=16, H_k=2, H_v=16, T=1, state_dtype=sd, num_slots=128, q_lens="ragged",
+                           pad_prob=0.1, seed=36)
+    pool0 = make_pool(case, cuda_device)
+    res = []
+    for flags in (0, 1, 3, 5, 7):
+        out, pool, st = run_gpu(case, cuda_device, pool0.clone(), split=0, flags=flags)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        res.append((out.view(torch.int16).clone(), pool.view(torch.int16).clone()))
+    for r in res[1:]:
+        assert torch.equal(r[0], res[0][0]) and torch.equal(r[1], res[0][1])
+
+
 @pytest.mark.parametrize("split", SPLITS)
 def test_ungated_raw_readout(cuda_device, split):
     """z = norm_w = NULL: out is the raw readout o, which the RMSNorm would
