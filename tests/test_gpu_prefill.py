@@ -263,6 +263,28 @@ def test_input_extremes(entry):
     _check(entry, ext, *_run(entry, ext, reads, writes), writes)
 
 
+@pytest.mark.parametrize("lens", [[200, 65, 1], [200, 65, 1] * 30], ids=["2-cta-units", "1-cta-units"])
+def test_chunked_runs_are_bit_identical(lens):
+    """Two calls on the same inputs give the same out and pool bits (no
+    atomics or order-dependent reductions in either launch form)."""
+    case = _case(lens, synth.BF16, H_k=1, H_v=8, seed=70)
+    reads, writes = _slots(case, 12, zero_every=10 ** 6, skip_every=10 ** 6)
+    pool0 = make_pool(case, DEV, slots=sorted(s for s in set(reads.tolist()) | set(writes.tolist()) if s >= 0))
+    t = device_tensors(case, DEV)
+    res = []
+    for _ in range(2):
+        pool = pool0.clone()
+        out = torch.zeros(case.num_tokens, case.H_v, case.V, dtype=torch.bfloat16, device=DEV)
+        st = torch.zeros(1, dtype=torch.int32, device=DEV)
+        gdn.gdn_prefill_chunked(t["q"], t["k"], t["v"], t["a"], t["b"], t["z"], t["A_log"], t["dt_bias"],
+                                t["norm_w"], pool, torch.from_numpy(reads).to(DEV), torch.from_numpy(writes).to(DEV),
+                                t["cu_seqlens"], out, scale=case.scale, eps=case.eps, status=st)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        res.append((out.view(torch.int16).clone(), pool.view(torch.int16).clone()))
+    assert torch.equal(res[0][0], res[1][0]) and torch.equal(res[0][1], res[1][1])
+
+
 @pytest.mark.parametrize("lens", [[100, 30], [100, 30] * 5], ids=["2-cta-units", "1-cta-units"])
 def test_wait_timeout_is_flagged_and_the_next_launch_is_clean(lens):
     """A wait bound of one poll runs out on the first tensor-core wait: the
