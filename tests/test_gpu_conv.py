@@ -108,9 +108,9 @@ def test_state_dtypes(sd):
 
 @pytest.mark.parametrize("ratio", [1, 2, 3, 4, 8])
 def test_head_ratios(ratio):
-    """H_v = ratio * H_k: ratios 2, 4 and 8 share the key head's q / k
-    convolution over a cluster of its v-heads (each CTA convolves a slice and
-    the cluster exchanges them); 1 and 3 convolve q / k in every CTA."""
+    """H_v = ratio * H_k: every CTA convolves its key head's q / k channels
+    itself (v-head h reads key head h / ratio); the new conv slot's q / k
+    channels are written by the key head's first v-head only."""
     case = _case(batch=5, H_k=2, H_v=2 * ratio, seed=90 + ratio)
     Step(case, synth.conv_inputs(case, seed=14 + ratio)).run().check()
 

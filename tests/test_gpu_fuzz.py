@@ -1,7 +1,8 @@
 """Seeded randomised configurations against the oracle: the decode step over
 batch sizes, head ratios, draft depths, acceptance and padding patterns,
-gathered rows, state dtypes and every split code, and the chunked prefill over
-prompt-length mixes, head ratios and state dtypes.  Each configuration is
+gathered rows, state dtypes and every split code; the chunked prefill over
+prompt-length mixes, head ratios and state dtypes; and the fused-conv step
+over widths, bias, head ratios, lengths, padding, gathers and flags.  Each configuration is
 drawn from a fixed seed, so a failure names a reproducible case."""
 from __future__ import annotations
 
@@ -71,3 +72,31 @@ def test_chunked_prefill_random_configuration(seed):
     reads, writes = _slots(case, s)
     for entry in ("chunked", "recurrent"):
         _check(entry, case, *_run(entry, case, reads, writes), writes)
+
+
+def _conv_config(seed):
+    rng = np.random.default_rng(5000 + seed)
+    H_k = int(rng.choice([1, 2, 3]))
+    ratio = int(rng.choice([1, 2, 3, 4, 8]))
+    T = int(rng.integers(1, 9))
+    batch = int(rng.integers(1, 25))
+    return dict(batch=batch, H_k=H_k, H_v=H_k * ratio, T=T, state_dtype=int(rng.choice(DTYPES)),
+                num_slots=2 * batch * T + 8, q_lens=rng.choice([None, "ragged"]),
+                pad_prob=float(rng.choice([0.0, 0.1])), extra_rows=int(rng.choice([0, 0, 9])),
+                seed=6000 + seed), int(rng.integers(1, 5)), bool(rng.random() > 0.3), int(rng.choice([0, 1, 3, 7]))
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_conv_random_configuration(seed):
+    """One random fused-conv step (width 1-4, bias or none, head ratios,
+    draft depth, ragged lengths, padded slots, gathered rows, state dtype,
+    early-read flags) against the oracle; the new conv slots bit for bit."""
+    from tests.gpu_util import active_rows
+    from tests.test_gpu_conv import Step
+    kw, width, bias, flags = _conv_config(seed)
+    case = synth.make_case(**kw)
+    if not len(active_rows(case)):                     # nothing to compare: every sequence skipped
+        kw.update(q_lens=None, pad_prob=0.0)
+        case = synth.make_case(**kw)
+    ci = synth.conv_inputs(case, width=width, with_bias=bias, seed=7000 + seed)
+    Step(case, ci).run(flags=flags).check()
