@@ -285,6 +285,40 @@ def test_chunked_runs_are_bit_identical(lens):
     assert torch.equal(res[0][0], res[1][0]) and torch.equal(res[0][1], res[1][1])
 
 
+@pytest.mark.parametrize("lens", [[200, 65, 1], [200, 65, 1] * 30], ids=["2-cta-units", "1-cta-units"])
+def test_chunked_in_a_cuda_graph(lens):
+    """The chunked prefill captured in a CUDA graph on a side stream (the
+    2-CTA cluster launch included) and replayed gives the bits of a direct
+    call."""
+    case = _case(lens, synth.F32, H_k=1, H_v=8, seed=71)
+    reads, writes = _slots(case, 13, zero_every=10 ** 6, skip_every=10 ** 6)
+    pool0 = make_pool(case, DEV, slots=sorted(s for s in set(reads.tolist()) | set(writes.tolist()) if s >= 0))
+    t = device_tensors(case, DEV)
+    r_dev, w_dev = torch.from_numpy(reads).to(DEV), torch.from_numpy(writes).to(DEV)
+
+    def call(pool, out, stream=None):
+        gdn.gdn_prefill_chunked(t["q"], t["k"], t["v"], t["a"], t["b"], t["z"], t["A_log"], t["dt_bias"],
+                                t["norm_w"], pool, r_dev, w_dev, t["cu_seqlens"], out, scale=case.scale,
+                                eps=case.eps, stream=stream)
+
+    direct_pool = pool0.clone()
+    direct_out = torch.zeros(case.num_tokens, case.H_v, case.V, dtype=torch.bfloat16, device=DEV)
+    call(direct_pool, direct_out)
+    torch.cuda.synchronize()
+    graph_pool = pool0.clone()
+    graph_out = torch.zeros_like(direct_out)
+    side = torch.cuda.Stream(DEV)
+    side.wait_stream(torch.cuda.current_stream(DEV))
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        call(graph_pool, graph_out, stream=side.cuda_stream)
+    graph_pool.copy_(pool0)
+    graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(graph_out.view(torch.int16), direct_out.view(torch.int16))
+    assert torch.equal(graph_pool.view(torch.int32), direct_pool.view(torch.int32))
+
+
 @pytest.mark.parametrize("lens", [[100, 30], [100, 30] * 5], ids=["2-cta-units", "1-cta-units"])
 def test_wait_timeout_is_flagged_and_the_next_launch_is_clean(lens):
     """A wait bound of one poll runs out on the first tensor-core wait: the
